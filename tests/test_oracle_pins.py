@@ -1,0 +1,359 @@
+"""Pins of the fp64 oracle to things other than itself.
+
+Each check is chosen so that a plausible slip in the oracle (a dropped term, a
+swapped channel or mean/std, a transposed axis, a wrong merge order, a wrong
+rotary width) fails at least one of them:
+
+* FusedInputNorm: hand-computed values of special parameter sets and the
+  zero crossing of the real constants;
+* patchify: brute-force nested-loop enumeration from the closed-form row and
+  feature index on tiny position-coded items, a hand-derived golden row order,
+  and the merge=1 case against plain raster img2col slicing;
+* patch embed: a direct Conv3d (kernel == stride) sum on tiny items, a one-hot
+  weight that must return the normalised pixels exactly, and the constant
+  colour closed form;
+* position ids: a hand-derived golden sequence and the closed-form index;
+* RoPE: pos 0, frequency index 0, the theta^(-1/2) frequency, geometric
+  frequency ratio, angle addition between neighbouring positions,
+  cos^2 + sin^2 = 1, the [H || W] layout and pad rows.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from vit_vision_encoder_fusedinputnorm_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([int(v) for v in line.split()])
+    return np.array(rows, dtype=np.int64)
+
+
+# ---------------------------------------------------------------- normalise
+
+def test_normalize_identity_parameters():
+    v = np.arange(256, dtype=np.uint8).reshape(1, 1, 256, 1).repeat(3, axis=3)
+    x = oracle.normalize(v, (0, 0, 0), (1, 1, 1), 1.0)
+    assert np.array_equal(x[..., 0].ravel(), np.arange(256, dtype=np.float64))
+    assert np.array_equal(x[..., 2].ravel(), np.arange(256, dtype=np.float64))
+
+
+def test_normalize_minus_one_to_one():
+    # mean 0.5, std 0.5 after 1/255: 0 -> -1, 255 -> +1, 51 -> -0.6.
+    v = np.array([[[[0, 255, 51]]]], dtype=np.uint8)
+    x = oracle.normalize(v, (0.5, 0.5, 0.5), (0.5, 0.5, 0.5), 1 / 255)
+    assert np.allclose(x.ravel(), [-1.0, 1.0, -0.6], atol=1e-15)
+
+
+def test_normalize_per_channel_hand_values():
+    # v = 40 in every channel, mean (0, 10, 20), std (1, 2, 4), rescale 1:
+    # channel 0 -> 40, channel 1 -> 15, channel 2 -> 5 (computed by hand).
+    v = np.full((1, 1, 1, 3), 40, dtype=np.uint8)
+    x = oracle.normalize(v, (0, 10, 20), (1, 2, 4), 1.0)
+    assert x.ravel().tolist() == [40.0, 15.0, 5.0]
+
+
+def test_normalize_zero_crossing_of_clip_constants():
+    # mean_c / rescale = 122.78, 116.74, 104.09: the sign flips between these bytes.
+    lo = np.array([[[[122, 116, 104]]]], dtype=np.uint8)
+    hi = np.array([[[[123, 117, 105]]]], dtype=np.uint8)
+    xl = oracle.normalize(lo, synth.QWEN_MEAN, synth.QWEN_STD, synth.RESCALE).ravel()
+    xh = oracle.normalize(hi, synth.QWEN_MEAN, synth.QWEN_STD, synth.RESCALE).ravel()
+    assert np.all(xl < 0) and np.all(xh > 0)
+    # slope per channel is rescale / std_c
+    assert np.allclose(xh - xl, [1 / 255 / 0.2686, 1 / 255 / 0.2613, 1 / 255 / 0.2758], rtol=1e-12)
+
+
+def test_normalize_rejects_non_uint8():
+    with pytest.raises(TypeError):
+        oracle.normalize(np.zeros((1, 1, 1, 3), np.float32), (0, 0, 0), (1, 1, 1), 1.0)
+
+
+# ---------------------------------------------------------------- patchify
+
+def _brute_force_rows(x, t, h, w, P, T, m):
+    """Nested loops from the closed-form indices (independent of reshape)."""
+    F = x.shape[0]
+    K = 3 * T * P * P
+    out = np.zeros((t * h * w, K), dtype=x.dtype)
+    for r in range(t * h * w):
+        tg, rem = divmod(r, h * w)
+        g, within = divmod(rem, m * m)
+        hb, wb = divmod(g, w // m)
+        mh, mw = divmod(within, m)
+        hh, ww = hb * m + mh, wb * m + mw
+        for c in range(3):
+            for tt in range(T):
+                f = 0 if F == 1 else tg * T + tt
+                for ph in range(P):
+                    for pw in range(P):
+                        k = ((c * T + tt) * P + ph) * P + pw
+                        out[r, k] = x[f, hh * P + ph, ww * P + pw, c]
+    return out
+
+
+@pytest.mark.parametrize("t,h,w,F,P,T,m", [
+    (1, 2, 2, 1, 14, 2, 2),     # 28 x 28 still
+    (1, 2, 4, 1, 14, 2, 2),     # 28 x 56
+    (1, 4, 6, 1, 14, 2, 2),     # 56 x 84
+    (2, 2, 4, 4, 14, 2, 2),     # 4-frame video 28 x 56
+    (1, 2, 4, 1, 16, 2, 2),     # 32 x 64, patch 16
+    (1, 6, 3, 1, 4, 2, 3),      # merge 3
+    (3, 2, 2, 3, 4, 1, 2),      # temporal patch 1, 3 frames
+])
+def test_patchify_brute_force(t, h, w, F, P, T, m):
+    x = synth.position_coded_image(F, h * P, w * P)
+    got = oracle.patchify(x, t, h, w, P, T, m)
+    exp = _brute_force_rows(x, t, h, w, P, T, m)
+    assert got.shape == (t * h * w, 3 * T * P * P)
+    assert np.array_equal(got, exp)
+
+
+def test_patch_row_order_golden():
+    g = _golden("patch_rows_h2_w4_m2.txt")
+    for merge in (2, 1):
+        exp = g[g[:, 0] == merge][:, 1:]
+        coords = oracle.patch_coords(1, 2, 4, merge)
+        assert np.array_equal(coords[:, 1:], exp)
+        # and the patchified rows hold exactly those patches
+        P = 2
+        x = synth.position_coded_image(1, 2 * P, 4 * P)
+        rows = oracle.patchify(x, 1, 2, 4, P, 2, merge)
+        for r, (hh, ww) in enumerate(exp):
+            blk = x[0, hh * P:(hh + 1) * P, ww * P:(ww + 1) * P, :]       # [P][P][C]
+            ref = np.stack([blk, blk], 0).transpose(3, 0, 1, 2).ravel()   # (C, T, P, P)
+            assert np.array_equal(rows[r], ref)
+
+
+def test_patchify_merge1_is_raster_img2col():
+    t, h, w, P, T = 1, 3, 5, 4, 2
+    x = synth.position_coded_image(1, h * P, w * P)
+    rows = oracle.patchify(x, t, h, w, P, T, 1)
+    r = 0
+    for hh in range(h):
+        for ww in range(w):
+            blk = x[0, hh * P:(hh + 1) * P, ww * P:(ww + 1) * P, :].transpose(2, 0, 1)  # C,P,P
+            exp = np.stack([blk, blk], axis=1).ravel()                                 # C,T,P,P
+            assert np.array_equal(rows[r], exp)
+            r += 1
+
+
+def test_patchify_counts_and_errors():
+    x = np.zeros((1, 56, 84, 3), np.uint8)
+    assert oracle.patchify(x, 1, 4, 6, 14, 2, 2).shape == (24, 1176)
+    with pytest.raises(ValueError):
+        oracle.patchify(np.zeros((1, 42, 84, 3), np.uint8), 1, 3, 6, 14, 2, 2)   # h not multiple of m
+    with pytest.raises(ValueError):
+        oracle.patchify(np.zeros((3, 28, 28, 3), np.uint8), 1, 2, 2, 14, 2, 2)   # frames != t*T
+
+
+def test_workload_row_counts():
+    # grid_thw counts: (H/P)(W/P) t per item.
+    assert synth.make_workload(0, with_pixels=False).live_rows == 256
+    assert synth.make_workload(1, with_pixels=False).live_rows == 18048
+    assert synth.make_workload(2, with_pixels=False).live_rows == 589824
+    w3 = synth.make_workload(3, with_pixels=False)
+    assert (w3.items[0].t, w3.items[0].h, w3.items[0].w) == (16, 32, 56)
+    assert w3.live_rows == 45056
+    w4 = synth.make_workload(4, with_pixels=False)
+    assert w4.K == 1536 and w4.hidden == 1152
+    for b in w4.buckets:
+        assert sum(w4.items[i].rows for i in b) <= 65536
+    assert sum(len(b) for b in w4.buckets) == 50
+
+
+# ---------------------------------------------------------------- embed
+
+def _closed_form_row(tg, hh, ww, h, w, m):
+    hb, mh = divmod(hh, m)
+    wb, mw = divmod(ww, m)
+    return ((tg * (h // m) + hb) * (w // m) + wb) * m * m + mh * m + mw
+
+
+@pytest.mark.parametrize("t,h,w,F", [(1, 2, 4, 1), (2, 2, 2, 4)])
+def test_embed_equals_direct_conv3d(t, h, w, F):
+    P, T, m, N = 4, 2, 2, 5
+    rng = np.random.default_rng(7)
+    x = rng.integers(0, 256, size=(F, h * P, w * P, 3), dtype=np.uint8)
+    W = synth.f32_to_bf16_bits(rng.standard_normal((N, 3 * T * P * P)).astype(np.float32) * 0.05)
+    b = synth.f32_to_bf16_bits(rng.standard_normal(N).astype(np.float32) * 0.05)
+    # identity normalisation (pinned above), so the conv sees the raw pixel values
+    y = oracle.embed_item(x, t, h, w, W, b, patch=P, tpatch=T, merge=m, mean=(0, 0, 0),
+                          std=(1, 1, 1), rescale=1.0)
+    W5 = oracle.bf16_bits_to_f64(W).reshape(N, 3, T, P, P)
+    conv = _direct_conv3d_float(x.astype(np.float64), t, h, w, P, T, W5,
+                                oracle.bf16_bits_to_f64(b))
+    for tg in range(t):
+        for hh in range(h):
+            for ww in range(w):
+                r = _closed_form_row(tg, hh, ww, h, w, m)
+                assert np.allclose(y[r], conv[tg, hh, ww], rtol=1e-12, atol=1e-12)
+
+
+def _direct_conv3d_float(xf, t, h, w, P, T, W5, bias):
+    F = xf.shape[0]
+    X = xf.transpose(0, 3, 1, 2)
+    N = W5.shape[0]
+    out = np.zeros((t, h, w, N))
+    for tg in range(t):
+        frames = [0] * T if F == 1 else [tg * T + tt for tt in range(T)]
+        for hh in range(h):
+            for ww in range(w):
+                blk = np.stack([X[f, :, hh * P:(hh + 1) * P, ww * P:(ww + 1) * P] for f in frames],
+                               axis=1)
+                for n in range(N):
+                    acc = 0.0
+                    for idx in np.ndindex(blk.shape):
+                        acc += W5[(n,) + idx] * blk[idx]
+                    out[tg, hh, ww, n] = acc + bias[n]
+    return out
+
+
+def test_embed_one_hot_weight_returns_pixels():
+    # W[n][k] = [k == k_n], b = 0, identity normalisation: y[:, n] = A[:, k_n] = a pixel value.
+    P, T, m = 4, 2, 2
+    K = 3 * T * P * P
+    ks = [0, 1, 17, K // 2, K - 1]
+    W = np.zeros((len(ks), K), np.uint16)
+    for n, k in enumerate(ks):
+        W[n, k] = 0x3F80                       # bf16 1.0
+    x = synth.position_coded_image(1, 2 * P, 4 * P)
+    y = oracle.embed_item(x, 1, 2, 4, W, None, patch=P, tpatch=T, merge=m, mean=(0, 0, 0),
+                          std=(1, 1, 1), rescale=1.0)
+    for n, k in enumerate(ks):
+        c, rest = divmod(k, T * P * P)
+        tt, rest = divmod(rest, P * P)
+        ph, pw = divmod(rest, P)
+        for r in range(8):              # grid 2 x 4, merge 2: one merge row of two units
+            wb, within = divmod(r, 4)
+            mh, mw = divmod(within, 2)
+            hh, ww = mh, wb * 2 + mw
+            assert y[r, n] == x[0, hh * P + ph, ww * P + pw, c]
+
+
+def test_embed_constant_colour_closed_form():
+    P, T, m, N = 4, 2, 2, 6
+    rng = np.random.default_rng(3)
+    W = synth.f32_to_bf16_bits(rng.standard_normal((N, 3 * T * P * P)).astype(np.float32) * 0.02)
+    b = synth.f32_to_bf16_bits(rng.standard_normal(N).astype(np.float32) * 0.02)
+    col = (200, 17, 90)
+    x = np.empty((1, 2 * P, 2 * P, 3), np.uint8)
+    x[...] = col
+    y = oracle.embed_item(x, 1, 2, 2, W, b, patch=P, tpatch=T, merge=m, mean=synth.QWEN_MEAN,
+                          std=synth.QWEN_STD, rescale=synth.RESCALE)
+    Wf = oracle.bf16_bits_to_f64(W).reshape(N, 3, -1).sum(axis=2)        # per-channel weight sums
+    xc = [(col[c] / 255.0 - synth.QWEN_MEAN[c]) / synth.QWEN_STD[c] for c in range(3)]
+    exp = Wf @ np.array(xc) + oracle.bf16_bits_to_f64(b)
+    assert np.allclose(y, exp[None, :], rtol=1e-12, atol=1e-13)
+
+
+def test_embed_linear_in_weight_and_bias():
+    P, T, m = 4, 2, 2
+    rng = np.random.default_rng(5)
+    x = rng.integers(0, 256, size=(1, 2 * P, 2 * P, 3), dtype=np.uint8)
+    W1 = synth.f32_to_bf16_bits(rng.standard_normal((3, 96)).astype(np.float32))
+    W2 = synth.f32_to_bf16_bits(rng.standard_normal((3, 96)).astype(np.float32))
+    kw = dict(patch=P, tpatch=T, merge=m, mean=(0.1, 0.2, 0.3), std=(0.5, 0.6, 0.7), rescale=0.01)
+    y1 = oracle.embed_item(x, 1, 2, 2, W1, None, **kw)
+    y2 = oracle.embed_item(x, 1, 2, 2, W2, None, **kw)
+    W12 = synth.f32_to_bf16_bits(oracle.bf16_bits_to_f64(W1).astype(np.float32)
+                                 + oracle.bf16_bits_to_f64(W2).astype(np.float32))
+    y12 = oracle.embed_item(x, 1, 2, 2, W12, None, **kw)
+    # W1 + W2 rounded to bf16: compare within bf16 rounding of the weights
+    assert np.allclose(y12, y1 + y2, rtol=2e-2, atol=2e-2)
+
+
+def test_embed_workload_sample_and_bucket():
+    wl = synth.small_workload(11, [(1, 2, 4, 1), (2, 2, 2, 4), (1, 4, 2, 1)], patch=4, hidden=8)
+    full = oracle.embed_workload(wl, bucket_rows=40)
+    assert full.shape == (40, 8)
+    assert np.all(full[wl.live_rows:] == 0)
+    s = np.array([0, 5, 9, 8, 23, 17])
+    assert np.array_equal(oracle.embed_workload(wl, sample=s), full[s])
+
+
+# ---------------------------------------------------------------- position ids
+
+def test_pos_ids_golden():
+    assert np.array_equal(oracle.pos_ids(2, 2, 4, 2), _golden("pos_ids_t2_h2_w4_m2.txt"))
+
+
+@pytest.mark.parametrize("t,h,w,m", [(1, 16, 16, 2), (3, 4, 10, 2), (1, 6, 9, 3), (2, 5, 7, 1)])
+def test_pos_ids_closed_form(t, h, w, m):
+    p = oracle.pos_ids(t, h, w, m)
+    for tg in range(t):
+        for hh in range(h):
+            for ww in range(w):
+                r = _closed_form_row(tg, hh, ww, h, w, m)
+                assert tuple(p[r]) == (hh, ww)
+
+
+def test_pos_ids_agree_with_patch_coords():
+    c = oracle.patch_coords(3, 4, 6, 2)
+    assert np.array_equal(oracle.pos_ids(3, 4, 6, 2), c[:, 1:])
+
+
+# ---------------------------------------------------------------- RoPE
+
+def test_rope_position_zero_is_identity():
+    cos, sin = oracle.rope_tables(np.zeros((3, 2), np.int64), 80, 10000.0)
+    assert cos.shape == (3, 40)
+    assert np.all(cos == 1.0) and np.all(sin == 0.0)
+
+
+def test_rope_first_frequency_is_position():
+    pos = np.array([[5, 11], [0, 95]])
+    cos, sin = oracle.rope_tables(pos, 80, 10000.0)
+    assert cos[0, 0] == pytest.approx(math.cos(5), abs=1e-15)
+    assert sin[0, 20] == pytest.approx(math.sin(11), abs=1e-15)
+    assert sin[1, 20] == pytest.approx(math.sin(95), abs=1e-15)
+
+
+def test_rope_middle_frequency_closed_form():
+    # head_dim 80: rotary width 40, i = 10 gives theta^(-20/40) = 1/100 for theta 1e4.
+    pos = np.array([[37, 3]])
+    cos, sin = oracle.rope_tables(pos, 80, 10000.0)
+    assert cos[0, 10] == pytest.approx(math.cos(0.37), abs=1e-15)
+    assert sin[0, 30] == pytest.approx(math.sin(0.03), abs=1e-15)
+
+
+def test_rope_geometric_frequencies_and_width():
+    for head_dim, ratio in [(80, 10000 ** (-1 / 20)), (72, 10000 ** (-1 / 18))]:
+        cos, sin = oracle.rope_tables(np.array([[1, 1]]), head_dim, 10000.0)
+        assert cos.shape[1] == head_dim // 2
+        ang = np.arctan2(sin[0, :head_dim // 4], cos[0, :head_dim // 4])
+        assert np.allclose(ang[1:] / ang[:-1], ratio, rtol=1e-12)
+
+
+def test_rope_angle_addition_between_positions():
+    pos = np.stack([np.arange(50), np.arange(50)[::-1]], 1)
+    cos, sin = oracle.rope_tables(pos, 80, 10000.0)
+    one_c, one_s = oracle.rope_tables(np.array([[1, 1]]), 80, 10000.0)
+    h = slice(0, 20)
+    # row p+1 (hpos) from row p and position 1
+    nc = cos[:-1, h] * one_c[0, h] - sin[:-1, h] * one_s[0, h]
+    assert np.allclose(nc, cos[1:, h], atol=1e-12)
+    assert np.allclose(cos ** 2 + sin ** 2, 1.0, atol=1e-14)
+
+
+def test_rope_layout_h_then_w_and_padding():
+    cos, sin = oracle.rope_tables(np.array([[0, 5], [-1, -1]]), 80, 10000.0)
+    assert np.all(cos[0, :20] == 1.0) and not np.any(cos[0, 20:] == 1.0)
+    assert np.all(cos[1] == 1.0) and np.all(sin[1] == 0.0)
+
+
+def test_rope_workload_rows_match_items():
+    wl = synth.small_workload(2, [(1, 2, 4, 1), (2, 2, 2, 4)], patch=4, hidden=8)
+    cos, sin = oracle.rope_workload(wl, bucket_rows=20)
+    assert cos.shape == (20, 40)
+    assert np.all(cos[wl.live_rows:] == 1.0)
