@@ -1,0 +1,349 @@
+"""Benchmark of the fused ViT front end (patch embeddings/s, % of dense bf16 peak).
+
+One step = one pass of the front end over 64 synthetic 1344x1344 stills
+(589,824 patches): the fused normalise + patchify + patch-embed GEMM + bias
+(vitfe_embed) and the 2D-RoPE tables (vitfe_rope), through the C ABI with
+inputs resident in device memory.  Inputs (347 MB of pixels) and outputs
+(1.51 GB of embeddings) exceed the 129 MB L2, so no flush is needed between
+iterations.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU: one process per GPU (torchrun); every rank runs the whole workload
+on its own GPU (items are independent, the weights are replicated), so scaling
+is weak and there is no data-path collective.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+CFG = 2
+METRIC = "patch embeddings/sec (uint8->bf16 hidden) and % of GB300 dense bf16 peak"
+UNIT = "patches/s"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0), "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ["vitfe_embed.cu", "vitfe_internal.cuh"]:
+        with open(os.path.join(ROOT, "vit_vision_encoder_fusedinputnorm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the embed kernel from the committed ncu summary, if current."""
+    p = os.path.join(ROOT, "profiles", "embed_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_hash") != source_hash():
+        return None
+    return d.get("dram_bytes_per_launch_full")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _oracle_strip(img: int, merge_rows: int):
+    """Time the oracle on the top ``merge_rows`` merge rows of image ``img`` of the workload."""
+    import dataclasses
+    import oracle
+    from vit_vision_encoder_fusedinputnorm_gb300 import synth
+    wl = synth.make_workload(CFG, item_subset=[img])
+    it = wl.items[img]
+    mr = min(merge_rows, it.h // wl.merge)
+    H = mr * wl.merge * wl.patch
+    strip = synth.Item(t=1, h=mr * wl.merge, w=it.w, frames=1, pixels=np.ascontiguousarray(it.pixels[:, :H]))
+    sub = dataclasses.replace(wl, items=[strip])
+    t0 = time.perf_counter()
+    oracle.embed_workload(sub)
+    return strip.rows, time.perf_counter() - t0
+
+
+def _cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    """The oracle as it stands, on this host's cores, on whole images of the workload."""
+    done, t_total, i = 0, 0.0, 0
+    while t_total < budget_s and i < 64:
+        n, dt = _oracle_strip(i, 10 ** 6)
+        done += n
+        t_total += dt
+        i += 1
+    return {"value": done / t_total, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+            "sample": f"{i} whole images of 64 ({done} patches): fp64 numpy oracle "
+                      f"(normalise, patchify, BLAS GEMM), {t_total:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The oracle timed as the reference arm: each step a strip of one image, sized so
+    the whole run stays within about two minutes."""
+    if rank != 0:
+        return 0
+    from vit_vision_encoder_fusedinputnorm_gb300 import synth
+    wl = synth.make_workload(CFG, with_pixels=False)
+    per_step = max(0.2, 100.0 / (args.steps + args.warmup))
+    n, dt = _oracle_strip(0, 4)                    # calibration
+    merge_rows = max(1, min(48, int(4 * per_step / max(dt, 1e-3))))
+    for w in range(args.warmup):
+        _oracle_strip(w % 64, merge_rows)
+    rates, rows_done, t_done = [], 0, 0.0
+    for k in range(args.steps):
+        n, dt = _oracle_strip(k % 64, merge_rows)
+        rates.append(n / dt)
+        rows_done += n
+        t_done += dt
+    v = rows_done / t_done
+    sample = (f"each step: top {merge_rows} merge rows ({merge_rows * 2 * 96} patches) of one 1344x1344 "
+              f"image, fp64 numpy oracle")
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": wl.live_rows / v * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "64 x 1344x1344 uint8 stills, patch 14, tpatch 2, merge 2, K 1176, N 1280",
+                       "rows_per_step": wl.live_rows},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": _cores(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+    from vit_vision_encoder_fusedinputnorm_gb300 import binding as B
+    from vit_vision_encoder_fusedinputnorm_gb300 import build as vbuild
+    from vit_vision_encoder_fusedinputnorm_gb300 import synth
+    from vit_vision_encoder_fusedinputnorm_gb300.frontend import FrontEnd
+
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        vbuild.build()
+    if world > 1:
+        dist.barrier()
+    B.load()
+
+    wl = synth.make_workload(CFG)
+    fe = FrontEnd.from_workload(wl, device=f"cuda:{local}")
+    batch = fe.upload(wl.items)
+    rows = batch.live_rows
+    N, K = wl.hidden, wl.K
+    out = torch.empty((rows, N), dtype=torch.bfloat16, device=dev)
+    cos = torch.empty((rows, wl.head_dim // 2), dtype=torch.float32, device=dev)
+    sin = torch.empty_like(cos)
+    st = torch.zeros(2, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        B.vitfe_embed(fe.h, batch.pixels, batch.pixel_bytes, batch.items, batch.n_items, batch.capacity, rows,
+                      out, st, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        B.vitfe_rope(fe.h, batch.items, batch.n_items, batch.capacity, rows, wl.head_dim, wl.theta, cos, sin,
+                     None, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    if st.cpu().tolist() != [0, -1]:
+        raise RuntimeError(f"device status {st.cpu().tolist()}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    total_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / args.steps
+    embed_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    rope_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    value = world * rows / (ms_step / 1e3)
+
+    # end to end through the C ABI from pinned host buffers: H2D pixels + items, the step,
+    # D2H of the embeddings and cos/sin tables.
+    host_px = torch.from_numpy(np.ascontiguousarray(batch.pixels.cpu().numpy())).pin_memory()
+    host_items = batch.items.cpu().pin_memory()
+    host_n = batch.n_items.cpu().pin_memory()
+    host_out = torch.empty((rows, N), dtype=torch.bfloat16).pin_memory()
+    host_cos = torch.empty(cos.shape, dtype=torch.float32).pin_memory()
+    host_sin = torch.empty(sin.shape, dtype=torch.float32).pin_memory()
+    h2d = host_px.numel() + host_items.numel() + 4
+    d2h = host_out.numel() * 2 + host_cos.numel() * 4 * 2
+
+    def e2e_step():
+        batch.pixels.copy_(host_px, non_blocking=True)
+        batch.items.copy_(host_items, non_blocking=True)
+        batch.n_items.copy_(host_n, non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+        host_cos.copy_(cos, non_blocking=True)
+        host_sin.copy_(sin, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    pk, pk_kind = peaks()
+    flops = 2.0 * rows * K * N
+    achieved = flops / (embed_ms / 1e3) / 1e12
+    peak = float(pk["bf16_tflops"])
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "64 x 1344x1344 uint8 stills, patch 14, tpatch 2, merge 2, K 1176, N 1280, "
+                               "RoPE head_dim 80", "rows_per_step": rows,
+                   "step": "vitfe_embed + vitfe_rope (C ABI, device-resident inputs)",
+                   "l2": "inputs (347 MB) and outputs (1.5 GB) exceed L2; no flush",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(),
+                     "peak_kind": f"{pk_kind} bf16 burst",
+                     "frac_of_sustained": achieved / float(pk.get("bf16_tflops_sustained", peak)),
+                     "kernel": "embed_kernel<14>", "flops_per_launch": flops,
+                     "kernel_ms": embed_ms},
+        "side_paths": {"rope_ms": rope_ms,
+                       "rope_gbs": rows * wl.head_dim // 2 * 4 * 2 / (rope_ms / 1e3) / 1e9},
+        "e2e": {"value": world * rows / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    fe.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,150 @@
+/*
+ * vitfe.h — C ABI of libvitfe, the GB300 (sm_103a) front end of a Qwen-VL
+ * style vision tower: FusedInputNorm + merge-order patchify + Conv3d patch
+ * embedding (as one tcgen05 GEMM with fused bias) + 2D-RoPE cos/sin tables.
+ *
+ * Sources of the operations (web pages, cited by title and section):
+ *  - "PR #55370 完整报告" ([Bugfix] Make mm_device_do_normalize
+ *    encoder-cudagraph safe, vLLM): 实现拆解 items 1-2 (normalisation is
+ *    owned by the vision tower's forward: integer pixels -> rescale ->
+ *    normalise -> model dtype), 评论区精华 item 1 (uint8-only input),
+ *    风险与影响 items 2-4 (no silent identity default; padding rows; the
+ *    per-replay cast and fp32 temporaries the fused path avoids).
+ *  - "vLLM 多模态推理｜ViT 性能优化": §2.2 (patchify in merge order,
+ *    flatten_patches, grid_thw, Conv3d patch embedding), §3.2 (the Conv3d as
+ *    an img2col GEMM; flatten_patches shapes), §3.3 (2D-RoPE cos/sin cache,
+ *    position ids in merge order, [H || W] concatenation).
+ *
+ * Conventions shared by every call:
+ *  - All tensors are caller-owned DEVICE memory unless a parameter says
+ *    "host".  Nothing here allocates, frees, synchronises or copies between
+ *    host and device except vitfe_create / vitfe_destroy, so vitfe_embed,
+ *    vitfe_rope, vitfe_normalize_patchify and vitfe_pos_ids can be captured
+ *    in a CUDA graph: per-call metadata (the item table and its count) is
+ *    read on the device at run time.
+ *  - A handle serialises its own work: calls that share a handle must be
+ *    ordered (one stream, or events between streams).
+ *  - Host-side argument errors return a status and launch nothing.
+ *    Device-side errors are written to the optional `status` word pair
+ *    (int32[2] = {code, item index or -1}); every device call overwrites it
+ *    ({0, -1} on success).  Rows of an item found invalid on the device are
+ *    written as the pad value; nothing is read out of range and nothing traps.
+ *  - Bucket padding: rows at or past sum(t*h*w) up to `rows` are written as
+ *    embedding 0, cos 1, sin 0, position id -1, flatten_patches 0.
+ *  - Pixel reads: the library reads whole aligned 4-byte words that overlap
+ *    an item's bytes, so it may touch up to 3 bytes past `pixel_bytes` but
+ *    never a word that holds none of the item's bytes.
+ */
+#ifndef VITFE_H
+#define VITFE_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>   /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VITFE_MAX_ITEMS 256      /* items per call (max_items bound)            */
+#define VITFE_ROPE_MAX_SIDE 4096 /* largest h or w (in patches) vitfe_rope takes */
+#define VITFE_ROPE_MAX_HEAD_DIM 512
+
+typedef struct vitfe_ctx* vitfe_t;
+
+typedef enum {
+  VITFE_OK = 0,
+  VITFE_EINVAL = 1,           /* host: bad argument, nothing launched            */
+  VITFE_ENOMEM = 2,           /* host: device allocation failed (create only)    */
+  VITFE_ECUDA = 3,            /* host: a CUDA runtime call failed                */
+  VITFE_EDEVICE_DESC = 4,     /* device: an item descriptor is inconsistent      */
+  VITFE_EDEVICE_RANGE = 5,    /* device: pixels past pixel_bytes, or rows > bucket */
+  VITFE_EDEVICE_TIMEOUT = 6,  /* device: a pipeline wait ran out; output invalid */
+  VITFE_EUNSUPPORTED = 7      /* host: shape the kernels do not implement        */
+} vitfe_status;
+
+/* One image or video (device-resident array, 24 bytes, 8-byte aligned).
+ * grid_thw = (t, h, w) in patches ("vLLM 多模态推理｜ViT 性能优化" §2.2).
+ * Pixels: uint8 [frames][h*patch][w*patch][3], HWC, contiguous, starting at
+ * `pixels + pixel_offset`.  frames == 1 marks a still (needs t == 1) that the
+ * temporal patch replicates; a video stores frames == t * tpatch.  h and w must
+ * be multiples of the merge size.  pixel_offset must be a multiple of 16. */
+typedef struct {
+  int64_t pixel_offset;
+  int32_t t, h, w;
+  int32_t frames;
+} vitfe_item;
+
+/* Create a handle for one model's front end.
+ * mean[3], std[3] (host): per-channel statistics; rescale: pixel scale (1/255).
+ *   x = (v * rescale - mean_c) / std_c  ("PR #55370 完整报告", 实现拆解 item 2).
+ *   std_c must be finite and > 0; there is no identity default.
+ * patch, tpatch, merge: P, T, m of the patchify (§2.2); hidden: N.
+ * W (device, bf16): Conv3d weight [hidden][3][tpatch][patch][patch] flattened to
+ *   [hidden][K], K = 3*tpatch*patch*patch (§3.2).  Copied: the caller may free it
+ *   after this returns.  b (device, bf16 [hidden]) or NULL for no bias.
+ * Limits: hidden % 16 == 0, 16 <= hidden <= 8192; patch 1..32; tpatch 1..4;
+ *   merge 1..8.  The call synchronises `stream` before returning.
+ * Returns VITFE_OK and *out, or an error (and *out = NULL). */
+vitfe_status vitfe_create(vitfe_t* out, const float mean[3], const float std[3], float rescale,
+                          int patch, int tpatch, int merge, int hidden,
+                          const void* W, const void* b, cudaStream_t stream);
+
+/* Release a handle (synchronises the device work it owns). NULL is ignored. */
+void vitfe_destroy(vitfe_t h);
+
+/* Fused FusedInputNorm + patchify + patch-embed GEMM + bias ("PR #55370
+ * 完整报告" 实现拆解 item 2; "vLLM 多模态推理｜ViT 性能优化" §2.2, §3.2).
+ * pixels (device uint8, 16-byte aligned), pixel_bytes: the pixel buffer.
+ * items (device vitfe_item[max_items]); n_items (device int32): live count,
+ *   0 <= *n_items <= max_items <= VITFE_MAX_ITEMS.
+ * rows: output rows (the bucket), >= 0.  out (device bf16 [rows][hidden],
+ *   16-byte aligned), row r = the r-th patch in item order, merge order inside
+ *   each item.  status (device int32[2]) or NULL.
+ * Normalised pixels and flatten_patches never reach device memory. */
+vitfe_status vitfe_embed(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes,
+                         const vitfe_item* items, const int32_t* n_items, int32_t max_items,
+                         int64_t rows, void* out, int32_t* status, cudaStream_t stream);
+
+/* 2D-RoPE tables ("vLLM 多模态推理｜ViT 性能优化" §3.3): rotary width
+ * d = head_dim / 2, inverse frequencies w_i = theta^(-2i/d), i < head_dim/4;
+ * cos[r] = [cos(hpos*w_i)]_i || [cos(wpos*w_i)]_i, sin likewise.
+ * cos, sin: device float32 [rows][head_dim/2], 16-byte aligned.
+ * head_dim % 8 == 0, 8 <= head_dim <= VITFE_ROPE_MAX_HEAD_DIM; theta > 0.
+ * Items with h or w > VITFE_ROPE_MAX_SIDE are rejected on the device. */
+vitfe_status vitfe_rope(vitfe_t h, const vitfe_item* items, const int32_t* n_items,
+                        int32_t max_items, int64_t rows, int head_dim, float theta,
+                        float* cos, float* sin, int32_t* status, cudaStream_t stream);
+
+/* Standalone FusedInputNorm + patchify: writes flatten_patches, bf16
+ * [rows][K] in the canonical (C, T, P, P) feature order of §3.2 (the order
+ * the Conv3d weight is flattened in).  Same inputs as vitfe_embed. */
+vitfe_status vitfe_normalize_patchify(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes,
+                                      const vitfe_item* items, const int32_t* n_items,
+                                      int32_t max_items, int64_t rows, void* out,
+                                      int32_t* status, cudaStream_t stream);
+
+/* Position ids (§3.3 step 2): int32 [rows][2] = (hpos, wpos) per patch in merge
+ * order, repeated over t; pad rows (-1, -1). */
+vitfe_status vitfe_pos_ids(vitfe_t h, const vitfe_item* items, const int32_t* n_items,
+                           int32_t max_items, int64_t rows, int32_t* pos, int32_t* status,
+                           cudaStream_t stream);
+
+/* Host helper: build packed item descriptors from grid_thw.
+ * grid_thw (host int32 [n][3]); is_still (host uint8 [n], nonzero = a still
+ * stored as one frame; NULL = every item with t == 1 is a still).
+ * Writes items_out (host [n]) with 16-byte aligned offsets of a packed pixel
+ * buffer, *total_rows = sum t*h*w, *pixel_bytes = bytes that buffer needs. */
+vitfe_status vitfe_items_from_grid(const int32_t* grid_thw, const uint8_t* is_still, int32_t n,
+                                   int patch, int tpatch, vitfe_item* items_out,
+                                   int64_t* total_rows, int64_t* pixel_bytes);
+
+/* Feature width K = 3*tpatch*patch*patch of a handle (0 for NULL). */
+int vitfe_feature_dim(vitfe_t h);
+
+/* Static description of a status code. */
+const char* vitfe_status_str(vitfe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VITFE_H */

@@ -1,0 +1,303 @@
+"""Parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bars: position ids bit-exact; normalised pixels within 1 bf16 ulp of the
+oracle's value rounded to bf16; embeddings within a relative Frobenius error of
+5e-3 per item and 2e-2 absolute; cos/sin within 1e-5 absolute.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from vit_vision_encoder_fusedinputnorm_gb300 import synth
+import vitfe_testutil as U
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from vit_vision_encoder_fusedinputnorm_gb300 import build
+    build.build()
+
+
+def _fe(wl):
+    from vit_vision_encoder_fusedinputnorm_gb300.frontend import FrontEnd
+    return FrontEnd.from_workload(wl)
+
+
+# small seeded cases: several 128-row tiles, ragged tails, mixed stills and video
+SMALL = {
+    "stills_p14": (14, 256, [(1, 2, 2, 1), (1, 4, 6, 1), (1, 16, 16, 1), (1, 10, 22, 1)]),
+    "mixed_p14": (14, 1280, [(2, 4, 6, 4), (1, 6, 8, 1), (3, 2, 4, 6), (1, 2, 2, 1)]),
+    "video_p14": (14, 512, [(4, 8, 10, 8)]),
+    "stills_p16": (16, 1152, [(1, 4, 4, 1), (1, 6, 10, 1), (2, 4, 2, 4)]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+@pytest.mark.parametrize("pad", [0, 300])
+def test_embed_small_vs_oracle(name, pad):
+    P, N, grids = SMALL[name]
+    wl = synth.small_workload(17, grids, patch=P, hidden=N, pixels="uniform")
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    rows = b.live_rows + pad
+    st = fe.status_tensor()
+    out = fe.embed(b, rows=rows, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, -1]
+    g = U.bits_to_f64(U.tensor_bits(out))
+    ref = oracle.embed_workload(wl, bucket_rows=rows)
+    rel, mx = U.embed_errors(g, ref, U.item_starts(wl.items))
+    assert rel <= U.EMBED_REL_FROB and mx <= U.EMBED_MAX_ABS, (rel, mx)
+    assert np.all(U.tensor_bits(out)[b.live_rows:] == 0)
+    fe.close()
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_normalize_patchify_within_one_ulp(name):
+    P, N, grids = SMALL[name]
+    wl = synth.small_workload(23, grids, patch=P, hidden=N, pixels="uniform")
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    rows = b.live_rows + 40
+    out = fe.normalize_patchify(b, rows=rows)
+    got = U.tensor_bits(out)
+    ref = U.f64_to_bf16_bits(oracle.normalize_patchify_workload(wl, bucket_rows=rows))
+    assert got.shape == ref.shape
+    assert int(U.ulp_distance(got, ref).max()) <= U.NORM_MAX_ULP
+    assert np.all(got[b.live_rows:] == 0)
+    fe.close()
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_pos_ids_and_rope(name):
+    P, N, grids = SMALL[name]
+    wl = synth.small_workload(5, grids, patch=P, hidden=N, head_dim=80 if P == 14 else 72)
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    rows = b.live_rows + 70
+    pos = fe.pos_ids(b, rows=rows).cpu().numpy()
+    assert np.array_equal(pos, oracle.pos_ids_workload(wl, bucket_rows=rows))
+    cos, sin = fe.rope(b, wl.head_dim, wl.theta, rows=rows)
+    rc, rs = oracle.rope_workload(wl, bucket_rows=rows)
+    assert np.max(np.abs(cos.cpu().numpy() - rc)) <= U.ROPE_MAX_ABS
+    assert np.max(np.abs(sin.cpu().numpy() - rs)) <= U.ROPE_MAX_ABS
+    fe.close()
+
+
+def test_one_hot_weight_returns_normalised_pixels_bit_exact():
+    # W[n][k] = [k == k_n], b = 0: every output equals bf16(x) for feature k_n, which pins
+    # the internal feature permutation and the row order bit-exactly against the
+    # standalone normalise + patchify path.
+    P, T = 14, 2
+    K = 3 * T * P * P
+    N = 128
+    ks = np.linspace(0, K - 1, N).astype(int)
+    W = np.zeros((N, K), np.uint16)
+    W[np.arange(N), ks] = 0x3F80
+    wl = synth.small_workload(9, [(1, 4, 6, 1), (2, 2, 4, 4), (1, 8, 2, 1)], patch=P, hidden=N)
+    wl.W_bits = W
+    wl.b_bits = None
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    emb = U.tensor_bits(fe.embed(b))
+    flat = U.tensor_bits(fe.normalize_patchify(b))
+    assert np.array_equal(emb, flat[:, ks])
+    fe.close()
+
+
+def test_still_equals_duplicated_two_frame_item():
+    # A still (one stored frame) and the same frame stored twice as a t=1 video item
+    # give the same embeddings up to fp32 summation order (resident vs streamed tiles).
+    wl = synth.small_workload(31, [(1, 8, 16, 1)], patch=14, hidden=1280)
+    px = wl.items[0].pixels
+    dup = synth.Item(t=1, h=8, w=16, frames=2, pixels=np.concatenate([px, px], 0))
+    fe = _fe(wl)
+    a = U.tensor_bits(fe.embed(fe.upload(wl.items)))
+    v = U.tensor_bits(fe.embed(fe.upload([dup])))
+    d = U.ulp_distance(a, v)
+    assert d.max() <= 1 and np.mean(d == 0) > 0.95
+    fe.close()
+
+
+def test_deterministic_rerun():
+    wl = synth.make_workload(1)
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    x = U.tensor_bits(fe.embed(b))
+    y = U.tensor_bits(fe.embed(b))
+    assert np.array_equal(x, y)
+    fe.close()
+
+
+def test_empty_and_all_pad_calls():
+    wl = synth.small_workload(3, [(1, 2, 2, 1)], patch=14, hidden=256)
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    b.n_items.zero_()
+    st = fe.status_tensor()
+    out = torch.full((300, 256), 7.0, dtype=torch.bfloat16, device="cuda")
+    fe.embed(b, rows=300, out=out, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, -1]
+    assert torch.count_nonzero(out).item() == 0
+    fe.embed(b, rows=0, status=st)          # nothing to write, status still set
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, -1]
+    fe.close()
+
+
+def test_device_side_descriptor_errors_zero_the_item_rows():
+    wl = synth.small_workload(13, [(1, 4, 4, 1), (1, 4, 6, 1), (1, 2, 2, 1)], patch=14, hidden=256)
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    good = U.tensor_bits(fe.embed(b))
+    # item 1: w not a multiple of the merge size
+    bad = b.host_items.copy()
+    bad[1]["w"] = 5
+    from vit_vision_encoder_fusedinputnorm_gb300 import binding as B
+    it, n = B.items_tensor(bad, device="cuda")
+    b.items = it
+    st = fe.status_tensor()
+    rows = 16 + 20 + 4
+    out = fe.embed(b, rows=rows, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [4, 1]
+    o = U.tensor_bits(out)
+    assert np.array_equal(o[:16], good[:16])
+    assert np.all(o[16:36] == 0)
+    assert np.array_equal(o[36:40], good[40:44])
+    # pixels beyond the buffer
+    bad2 = b.host_items.copy()
+    bad2[2]["pixel_offset"] = b.pixel_bytes
+    b.items, _ = B.items_tensor(bad2, device="cuda")
+    fe.embed(b, rows=44, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [5, 2]
+    # more rows than the bucket
+    b.items, _ = B.items_tensor(b.host_items, device="cuda")
+    fe.embed(b, rows=30, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [5, 1]
+    # count above capacity
+    b.n_items.fill_(99)
+    fe.embed(b, rows=44, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist()[0] == 4
+    fe.close()
+
+
+# --------------------------------------------------------------------------- full workloads
+
+@pytest.mark.parametrize("cfg", [0, 1, 3])
+def test_full_workload_embed(cfg):
+    wl = synth.make_workload(cfg)
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    out = fe.embed(b)
+    g = U.bits_to_f64(U.tensor_bits(out))
+    ref = oracle.embed_workload(wl)
+    rel, mx = U.embed_errors(g, ref, U.item_starts(wl.items))
+    assert rel <= U.EMBED_REL_FROB and mx <= U.EMBED_MAX_ABS, (rel, mx)
+    pos = fe.pos_ids(b).cpu().numpy()
+    assert np.array_equal(pos, oracle.pos_ids_workload(wl))
+    cos, sin = fe.rope(b, wl.head_dim, wl.theta)
+    rc, rs = oracle.rope_workload(wl)
+    assert np.max(np.abs(cos.cpu().numpy() - rc)) <= U.ROPE_MAX_ABS
+    assert np.max(np.abs(sin.cpu().numpy() - rs)) <= U.ROPE_MAX_ABS
+    fe.close()
+
+
+def test_throughput_workload_sampled():
+    # 64 x 1344^2 stills, in the launch configuration the benchmark times; sampled rows:
+    # both sides of every 128-row tile boundary plus random rows.
+    wl = synth.make_workload(2)
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    out = fe.embed(b)
+    rows = b.live_rows
+    rng = np.random.default_rng(0)
+    bnd = np.arange(128, rows, 128)
+    sample = np.unique(np.concatenate([bnd, bnd - 1, rng.integers(0, rows, 8192), [0, rows - 1]]))
+    g = U.bits_to_f64(U.tensor_bits(out[torch.from_numpy(sample).cuda()]))
+    ref = oracle.embed_workload(wl, sample=sample)
+    d = g - ref
+    rel = np.linalg.norm(d) / np.linalg.norm(ref)
+    assert rel <= U.EMBED_REL_FROB and np.max(np.abs(d)) <= U.EMBED_MAX_ABS, (rel, np.max(np.abs(d)))
+    pos = fe.pos_ids(b).cpu().numpy()
+    assert np.array_equal(pos, oracle.pos_ids_workload(wl))
+    flat = fe.normalize_patchify(b)
+    f = U.tensor_bits(flat[torch.from_numpy(sample[:2048]).cuda()])
+    # oracle rows for the sample from the items they fall in
+    starts = U.item_starts(wl.items)
+    ref_np = np.zeros((2048, wl.K))
+    for j, r in enumerate(sample[:2048]):
+        i = int(np.searchsorted(starts, r, side="right") - 1)
+        it = wl.items[i]
+        if j == 0 or i != last_i:
+            A = oracle.normalize_patchify_item(it.pixels, it.t, it.h, it.w, patch=wl.patch, tpatch=wl.tpatch,
+                                               merge=wl.merge, mean=wl.mean, std=wl.std, rescale=wl.rescale)
+            last_i = i
+        ref_np[j] = A[r - starts[i]]
+    assert int(U.ulp_distance(f, U.f64_to_bf16_bits(ref_np)).max()) <= U.NORM_MAX_ULP
+    fe.close()
+
+
+def test_graph_replay_bucket_masks_pad_rows():
+    # 50 varied stills (patch 16) packed into fixed 65,536-row buckets: one captured graph
+    # (embed + rope) replayed per bucket; live rows equal an eager call on exactly the live
+    # rows bit for bit, pad rows are masked, sampled rows match the oracle.
+    wl = synth.make_workload(4)
+    fe = _fe(wl)
+    R = wl.bucket_rows
+    from vit_vision_encoder_fusedinputnorm_gb300 import binding as B
+    packs = [B.pack_items([wl.items[i] for i in bk], wl.patch, wl.tpatch) for bk in wl.buckets]
+    cap_bytes = max(p[1].size for p in packs)
+    px = torch.zeros(cap_bytes, dtype=torch.uint8, device="cuda")
+    it_dev = torch.zeros(B.VITFE_MAX_ITEMS * 24, dtype=torch.uint8, device="cuda")
+    n_dev = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty((R, wl.hidden), dtype=torch.bfloat16, device="cuda")
+    cos = torch.empty((R, wl.head_dim // 2), dtype=torch.float32, device="cuda")
+    sin = torch.empty_like(cos)
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        B.vitfe_embed(fe.h, px, cap_bytes, it_dev, n_dev, B.VITFE_MAX_ITEMS, R, out, st, s)
+        B.vitfe_rope(fe.h, it_dev, n_dev, B.VITFE_MAX_ITEMS, R, wl.head_dim, wl.theta, cos, sin, None, s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        B.vitfe_embed(fe.h, px, cap_bytes, it_dev, n_dev, B.VITFE_MAX_ITEMS, R, out, st, s)
+        B.vitfe_rope(fe.h, it_dev, n_dev, B.VITFE_MAX_ITEMS, R, wl.head_dim, wl.theta, cos, sin, None, s)
+    rng = np.random.default_rng(4)
+    for bk, (items, buf, live) in zip(wl.buckets, packs):
+        px[:buf.size].copy_(torch.from_numpy(buf))
+        arr = np.zeros(B.VITFE_MAX_ITEMS, B.ITEM_DTYPE)
+        arr[:len(items)] = items
+        it_dev.copy_(torch.from_numpy(arr.view(np.uint8)))
+        n_dev.fill_(len(items))
+        out.fill_(3.0)
+        cos.fill_(5.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert st.cpu().tolist() == [0, -1]
+        o = U.tensor_bits(out)
+        assert np.all(o[live:] == 0)
+        c = cos.cpu().numpy()
+        assert np.all(c[live:] == 1.0) and np.all(sin.cpu().numpy()[live:] == 0.0)
+        # eager call on exactly the live rows
+        sub = synth.Workload(**{**wl.__dict__, "items": [wl.items[i] for i in bk], "bucket_rows": None,
+                                "buckets": None})
+        eb = fe.upload(sub.items)
+        e = U.tensor_bits(fe.embed(eb))
+        assert np.array_equal(o[:live], e)
+        sample = np.unique(rng.integers(0, live, 4096))
+        ref = oracle.embed_workload(sub, sample=sample)
+        rel, mx = U.embed_errors(U.bits_to_f64(o[sample]), ref, [0, len(sample)])
+        assert rel <= U.EMBED_REL_FROB and mx <= U.EMBED_MAX_ABS, (rel, mx)
+        rc, _ = oracle.rope_workload(sub)
+        assert np.max(np.abs(c[:live] - rc)) <= U.ROPE_MAX_ABS
+    fe.close()
