@@ -2,7 +2,9 @@
 
 Bars: position ids bit-exact; normalised pixels within 1 bf16 ulp of the
 oracle's value rounded to bf16; embeddings within a relative Frobenius error of
-5e-3 per item and 2e-2 absolute; cos/sin within 1e-5 absolute.
+5e-3 per item and 2e-2 absolute beyond the rounding of the exact value to the
+bf16 output (half a bf16 ulp, up to 0.031 for |y| >= 8, which no bf16 output can
+avoid); cos/sin within 1e-5 absolute.
 """
 import numpy as np
 import pytest
@@ -119,7 +121,10 @@ def test_still_equals_duplicated_two_frame_item():
     a = U.tensor_bits(fe.embed(fe.upload(wl.items)))
     v = U.tensor_bits(fe.embed(fe.upload([dup])))
     d = U.ulp_distance(a, v)
-    assert d.max() <= 1 and np.mean(d == 0) > 0.95
+    ad = np.abs(U.bits_to_f64(a) - U.bits_to_f64(v))
+    # differ only by fp32 summation order: at most one bf16 ulp, or a few ulps of values
+    # near zero (absolute difference at the fp32 accumulation level)
+    assert np.all((d <= 1) | (ad <= 1e-5)) and np.mean(d == 0) > 0.95
     fe.close()
 
 
@@ -201,7 +206,7 @@ def test_full_workload_embed(cfg):
     g = U.bits_to_f64(U.tensor_bits(out))
     ref = oracle.embed_workload(wl)
     rel, mx = U.embed_errors(g, ref, U.item_starts(wl.items))
-    assert rel <= U.EMBED_REL_FROB and mx <= U.EMBED_MAX_ABS, (rel, mx)
+    assert rel <= U.EMBED_REL_FROB and mx <= U.EMBED_MAX_ABS, (rel, mx, U.raw_max_abs(g, ref))
     pos = fe.pos_ids(b).cpu().numpy()
     assert np.array_equal(pos, oracle.pos_ids_workload(wl))
     cos, sin = fe.rope(b, wl.head_dim, wl.theta)
@@ -224,9 +229,8 @@ def test_throughput_workload_sampled():
     sample = np.unique(np.concatenate([bnd, bnd - 1, rng.integers(0, rows, 8192), [0, rows - 1]]))
     g = U.bits_to_f64(U.tensor_bits(out[torch.from_numpy(sample).cuda()]))
     ref = oracle.embed_workload(wl, sample=sample)
-    d = g - ref
-    rel = np.linalg.norm(d) / np.linalg.norm(ref)
-    assert rel <= U.EMBED_REL_FROB and np.max(np.abs(d)) <= U.EMBED_MAX_ABS, (rel, np.max(np.abs(d)))
+    rel, mx = U.embed_errors(g, ref, [0, len(sample)])
+    assert rel <= U.EMBED_REL_FROB and mx <= U.EMBED_MAX_ABS, (rel, mx, U.raw_max_abs(g, ref))
     pos = fe.pos_ids(b).cpu().numpy()
     assert np.array_equal(pos, oracle.pos_ids_workload(wl))
     flat = fe.normalize_patchify(b)

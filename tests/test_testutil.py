@@ -32,4 +32,10 @@ def test_embed_errors_per_item():
     g = ref.copy()
     g[4:] += 0.01
     rel, mx = U.embed_errors(g, ref, [0, 4, 6])
-    assert abs(rel - 0.01) < 1e-12 and abs(mx - 0.01) < 1e-12
+    # half a bf16 ulp at 1.0 is 2^-8
+    assert abs(rel - 0.01) < 1e-12 and abs(mx - (0.01 - 2 ** -8)) < 1e-12
+
+
+def test_half_ulp():
+    assert U.bf16_half_ulp(np.array([1.0, 1.5, 4.0, 7.9, 8.0, -5.0])).tolist() == \
+        [2 ** -8, 2 ** -8, 2 ** -6, 2 ** -6, 2 ** -5, 2 ** -6]
