@@ -179,6 +179,34 @@ def run_reference(args, rank, world):
     return 0
 
 
+def kernel_only(args):
+    """Small case for ncu captures: one entry point on the first ``images`` images."""
+    import torch
+    from vit_vision_encoder_fusedinputnorm_gb300 import build as vbuild
+    from vit_vision_encoder_fusedinputnorm_gb300 import synth
+    from vit_vision_encoder_fusedinputnorm_gb300.frontend import FrontEnd
+    vbuild.build()
+    wl = synth.make_workload(CFG, item_subset=list(range(args.images)))
+    wl.items = wl.items[:args.images]
+    fe = FrontEnd.from_workload(wl)
+    b = fe.upload(wl.items)
+    st = fe.status_tensor()
+    bufs = {}
+    for i in range(args.warmup + args.launches):
+        if args.kernel_only == "embed":
+            bufs["o"] = fe.embed(b, out=bufs.get("o"), status=st)
+        elif args.kernel_only == "rope":
+            c, s_ = fe.rope(b, wl.head_dim, wl.theta, cos=bufs.get("c"), sin=bufs.get("s"), status=st)
+            bufs["c"], bufs["s"] = c, s_
+        else:
+            bufs["o"] = fe.normalize_patchify(b, out=bufs.get("o"), status=st)
+    torch.cuda.synchronize()
+    if st.cpu().tolist() != [0, -1]:
+        raise RuntimeError(f"device status {st.cpu().tolist()}")
+    fe.close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -187,8 +215,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-only", choices=["embed", "rope", "normalize_patchify"],
+                    help="profiling mode: launch one entry point on a subset of the images, print nothing")
+    ap.add_argument("--images", type=int, default=64, help="images of the workload (profiling mode)")
+    ap.add_argument("--launches", type=int, default=3, help="launches after warm-up (profiling mode)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.kernel_only:
+        return kernel_only(args)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -100,7 +100,8 @@ void vitfe_destroy(vitfe_t h);
  * rows: output rows (the bucket), >= 0.  out (device bf16 [rows][hidden],
  *   16-byte aligned), row r = the r-th patch in item order, merge order inside
  *   each item.  status (device int32[2]) or NULL.
- * Normalised pixels and flatten_patches never reach device memory. */
+ * Normalised pixels and flatten_patches never reach device memory.
+ * Implemented for patch 14 or 16 and hidden % 64 == 0 (else VITFE_EUNSUPPORTED). */
 vitfe_status vitfe_embed(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes,
                          const vitfe_item* items, const int32_t* n_items, int32_t max_items,
                          int64_t rows, void* out, int32_t* status, cudaStream_t stream);

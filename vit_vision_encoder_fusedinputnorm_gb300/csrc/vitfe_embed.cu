@@ -6,14 +6,19 @@
 //     A[r][k]   = bf16( v * rescale/std_c - mean_c/std_c ),
 // where v is the uint8 pixel feature k of patch r.  A never reaches device memory.
 //
-// Structure (one persistent CTA per SM, 10 warps):
-//   warps 0-3  A producers: one thread per tile row gathers uint8 pixel runs with
-//              aligned 4-byte loads, normalises in fp32, rounds to bf16 and stores
-//              into 128-byte-swizzled K-major shared-memory blocks (64 features each);
-//   warp 8     TMA producer of W tiles (box 64 x bn, 128-byte swizzle);
-//   warp 9     TMEM allocator and the single MMA-issuing thread (tcgen05.mma kind::f16,
-//              M=128, N=bn, fp32 accumulators double-buffered in tensor memory);
-//   warps 4-7  epilogue: tcgen05.ld of the accumulator, + bias, bf16 RNE, stores.
+// Structure: persistent clusters of two CTAs (one per SM).  A pair owns 256-row tiles,
+// 128 rows per CTA; one tcgen05.mma.cta_group::2 (M=256) spans both CTAs' shared and
+// tensor memory, so each CTA holds only half of every W tile.  Per CTA, 14 warps:
+//   warps 0-3   A producers: one thread per tile row gathers uint8 pixel runs with
+//               aligned 4-byte loads, normalises in fp32, rounds to bf16 and stores
+//               into 128-byte-swizzled K-major shared-memory blocks (64 features each);
+//   warp 12     TMA producer of this CTA's half of each W tile (box 64 x bn/2);
+//   warp 13     tensor-memory allocation (both CTAs); in the even CTA one thread issues
+//               the MMAs (fp32 accumulators double-buffered in tensor memory);
+//   warps 4-11  epilogue, two warps per tensor-memory lane quarter (each half of the
+//               columns): tcgen05.ld of the accumulator, + bias, bf16 RNE, 256-bit stores.
+// Barriers that gather both CTAs (A ready, W tile ready, accumulator free) live in the
+// even CTA; the MMA's completion is multicast to both CTAs.
 //
 // Features inside one temporal slice are ordered (ph, pw, c) so that each patch row
 // of pixels is one contiguous byte run; the weight was permuted the same way once
@@ -29,11 +34,12 @@
 namespace vitfe {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr int kProducerThreads = 128;
-constexpr int kEpiWarp0 = 4;
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kEpilogueThreads = 256;     // two warps per tensor-memory lane quarter
+constexpr int kPairRows = 2 * kTileM;
+constexpr int kTmaWarp = 12;
+constexpr int kMmaWarp = 13;
 constexpr int kABlockBytes = kTileM * 128;   // 128 rows x 64 bf16
 
 enum TileKind : int { kPad = 0, kResident = 1, kStream = 2 };
@@ -53,7 +59,7 @@ struct EmbedArgs {
   int kslice_pad;
   int bn, nstage, npass;
   int tmem_cols;
-  int num_tiles;
+  int num_tiles;   // 256-row pair tiles
   uint64_t limit_ns;
 };
 
@@ -78,7 +84,7 @@ __device__ __forceinline__ int tile_kind(int r0, const SmemHdr* h, int T) {
   const int live = h->tab.live;
   if (r0 >= live) return kPad;
   if (T == 1) return kResident;
-  const int r1 = min(r0 + kTileM, live) - 1;
+  const int r1 = min(r0 + kPairRows, live) - 1;
   const int n = h->tab.n;
   const int i0 = find_item(h->start, n, r0);
   const int i1 = find_item(h->start, n, r1);
@@ -102,7 +108,7 @@ template <int P>
 __device__ __forceinline__ bool produce_slice(const uint8_t* base, int64_t rs, uint32_t a_smem,
                                               SmemHdr* hs, uint32_t np, int row, const float sc[3],
                                               const float sh[3], volatile int* abort_flag,
-                                              uint64_t limit_ns) {
+                                              uint64_t limit_ns, uint32_t a_full_leader) {
   constexpr int RUN = 3 * P;                 // bytes of one patch row of pixels
   constexpr int KS = 3 * P * P;
   constexpr int NBLK = (KS + 63) / 64;
@@ -123,7 +129,7 @@ __device__ __forceinline__ bool produce_slice(const uint8_t* base, int64_t rs, u
       const int j = kc >> 3;           // K block
       const int q = kc & 7;            // chunk inside the 128-byte row
       if (q == 0) {
-        if (!mbar_wait(smem_u32(&hs->a_empty[j]), empty_parity, abort_flag, limit_ns)) return false;
+        if (!mbar_wait_cl(smem_u32(&hs->a_empty[j]), empty_parity, abort_flag, limit_ns, 128)) return false;
       }
       const uint32_t addr = a_smem + (uint32_t)j * kABlockBytes + row_off + (((uint32_t)q ^ swz) << 4);
       asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(cw[0]), "r"(cw[1]),
@@ -131,27 +137,39 @@ __device__ __forceinline__ bool produce_slice(const uint8_t* base, int64_t rs, u
                    : "memory");
       const bool last_of_block = (q == 7) || (kc == KEND / 8 - 1);
       if (last_of_block) {
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&hs->a_full[j]));
+        fence_proxy_async_all();
+        mbar_arrive_cluster(a_full_leader + 8u * (uint32_t)j);
       }
     }
     return true;
   };
 
-#pragma unroll
-  for (int ph = 0; ph < P; ++ph) {
-    uint32_t al[NA];
+  // Loads of patch row ph+1 are issued before row ph is converted and stored, so the
+  // global-load latency overlaps the conversion instead of adding up over the P rows.
+  uint32_t raw[2][NW];
+  auto load_run = [&](int ph, uint32_t (&dst)[NW]) {
     if (base != nullptr) {
-      const uint8_t* src = base + (int64_t)ph * rs;
-      const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+      const uintptr_t a = reinterpret_cast<uintptr_t>(base + (int64_t)ph * rs);
       const uint32_t s = (uint32_t)(a & 3u);
       const uint32_t* w0 = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-      uint32_t raw[NW];
 #pragma unroll
-      for (int w = 0; w < NW; ++w) raw[w] = (4u * w < s + RUN) ? __ldg(w0 + w) : 0u;
-      const uint32_t sel = 0x3210u + 0x1111u * s;
+      for (int w = 0; w < NW; ++w) dst[w] = (4u * w < s + RUN) ? __ldg(w0 + w) : 0u;
+    }
+  };
+  const uint32_t sel = base ? 0x3210u + 0x1111u * (uint32_t)(reinterpret_cast<uintptr_t>(base) & 3u) : 0x3210u;
+  // all runs of a patch share the byte alignment only when rs is a multiple of 4; otherwise
+  // the selector is recomputed per row
+  const bool same_align = (rs & 3) == 0;
+  load_run(0, raw[0]);
 #pragma unroll
-      for (int w = 0; w < NA; ++w) al[w] = __byte_perm(raw[w], raw[w + 1], sel);
+  for (int ph = 0; ph < P; ++ph) {
+    if (ph + 1 < P) load_run(ph + 1, raw[(ph + 1) & 1]);
+    uint32_t al[NA];
+    if (base != nullptr) {
+      const uint32_t sl = same_align ? sel
+          : 0x3210u + 0x1111u * (uint32_t)(reinterpret_cast<uintptr_t>(base + (int64_t)ph * rs) & 3u);
+#pragma unroll
+      for (int w = 0; w < NA; ++w) al[w] = __byte_perm(raw[ph & 1][w], raw[ph & 1][w + 1], sl);
     } else {
 #pragma unroll
       for (int w = 0; w < NA; ++w) al[w] = 0u;
@@ -180,9 +198,60 @@ __device__ __forceinline__ bool produce_slice(const uint8_t* base, int64_t rs, u
   return true;
 }
 
+// 32 contiguous bytes (16 bf16) with one 256-bit store, evict-first.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// Where the A producer thread of a tile row reads its pixels.
+struct RowSrc {
+  const uint8_t* base0;   // slice 0 patch origin, nullptr for rows written as zeros
+  int64_t rs;             // bytes between pixel rows
+  int64_t fstride;        // bytes between the frames of consecutive slices (0 for stills)
+};
+
 template <int P>
-__global__ void __launch_bounds__(kThreads, 1) embed_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                                                            const EmbedArgs args) {
+__device__ __forceinline__ RowSrc row_src(const EmbedArgs& args, const SmemHdr* hs, int r) {
+  RowSrc src{nullptr, 0, 0};
+  if (r < hs->tab.live) {
+    const int i = find_item(hs->start, hs->tab.n, r);
+    if (!tab_bit(hs->bad, i)) {
+      const vitfe_item it = args.items[i];
+      int tg, hh, ww;
+      decode_local(r - hs->start[i], it.h, it.w, args.M, tg, hh, ww);
+      const int64_t H = (int64_t)it.h * P, W = (int64_t)it.w * P;
+      src.rs = W * 3;
+      const bool still = (it.frames == 1);
+      src.fstride = still ? 0 : H * W * 3;
+      const int64_t f0 = still ? 0 : (int64_t)tg * args.T;
+      src.base0 = args.pixels + it.pixel_offset + ((f0 * H + (int64_t)hh * P) * W + (int64_t)ww * P) * 3;
+    }
+  }
+  return src;
+}
+
+// Pull the pixel runs of a row into L2 ahead of its production (first and last byte of
+// every run of every slice the row reads).
+template <int P>
+__device__ __forceinline__ void prefetch_row(const RowSrc& src, int nslices) {
+  if (src.base0 == nullptr) return;
+  for (int sl = 0; sl < nslices; ++sl) {
+    const uint8_t* b = src.base0 + src.fstride * sl;
+#pragma unroll
+    for (int ph = 0; ph < P; ++ph) {
+      const uint8_t* a = b + (int64_t)ph * src.rs;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a + 3 * P - 1));
+    }
+    if (src.fstride == 0) break;
+  }
+}
+
+template <int P>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    embed_kernel(const __grid_constant__ CUtensorMap tmap_w, const EmbedArgs args) {
   constexpr int KS = 3 * P * P;
   constexpr int NBLK = (KS + 63) / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -191,17 +260,22 @@ __global__ void __launch_bounds__(kThreads, 1) embed_kernel(const __grid_constan
   const uint32_t tiles_base = (raw_base + (uint32_t)sizeof(SmemHdr) + 1023u) & ~1023u;
   const uint32_t a_smem = tiles_base;
   const uint32_t b_smem = tiles_base + NBLK * kABlockBytes;
-  const uint32_t b_stage_bytes = (uint32_t)args.bn * 128u;
+  const int bnh = args.bn / 2;                                   // W rows per CTA per tile
+  const uint32_t b_stage_bytes = (uint32_t)bnh * 128u;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
+  const int cid = (int)cluster_id_x();
+  const int ncl = (int)nclusters_x();
   volatile int* abort_flag = &hs->abort_flag;
 
   // ---- prologue -----------------------------------------------------------
   if (threadIdx.x == 0) {
     hs->abort_flag = 0;
     for (int j = 0; j < NBLK; ++j) {
-      mbar_init(smem_u32(&hs->a_full[j]), kProducerThreads);
+      mbar_init(smem_u32(&hs->a_full[j]), 2 * kProducerThreads);
       mbar_init(smem_u32(&hs->a_empty[j]), 1);
     }
     for (int s = 0; s < args.nstage; ++s) {
@@ -210,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) embed_kernel(const __grid_constan
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&hs->acc_full[b]), 1);
-      mbar_init(smem_u32(&hs->acc_empty[b]), kProducerThreads);
+      mbar_init(smem_u32(&hs->acc_empty[b]), 2 * kEpilogueThreads);
     }
     mbar_init(smem_u32(&hs->drain), 1);
     fence_mbar_init();
@@ -221,167 +295,188 @@ __global__ void __launch_bounds__(kThreads, 1) embed_kernel(const __grid_constan
                      args.rows, 0x7fffffff, tab);
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(&hs->tmem_base), (uint32_t)args.tmem_cols);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&hs->tmem_base), (uint32_t)args.tmem_cols);
+    tmem_relinquish_pair();
   }
   if (warp == kTmaWarp && lane == 0) tma_prefetch_desc(&tmap_w);
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   tc_fence_after();
   write_status(args.status, &hs->tab);
   const uint32_t tmem = hs->tmem_base;
+  // barriers of the even CTA, through the cluster shared window
+  const uint32_t a_full_L = mapa_shared(smem_u32(&hs->a_full[0]), 0);
+  const uint32_t b_full_L = mapa_shared(smem_u32(&hs->b_full[0]), 0);
+  const uint32_t acc_empty_L = mapa_shared(smem_u32(&hs->acc_empty[0]), 0);
 
   // ---- roles -------------------------------------------------------------
   if (warp < 4) {
-    // A producers
+    // A producers: this CTA's 128 rows of every pair tile
     const float sc[3] = {args.scale0, args.scale1, args.scale2};
     const float sh[3] = {args.shift0, args.shift1, args.shift2};
     const int row = threadIdx.x;
+    const int rofs = (int)rank * kTileM + row;
     uint32_t np = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
-      const int r0 = tile * kTileM;
-      const int kind = tile_kind(r0, hs, args.T);
-      if (kind == kPad) continue;
-      const int r = r0 + row;
-      const uint8_t* base0 = nullptr;
-      int64_t rs = 0, fstride = 0;
-      if (r < hs->tab.live) {
-        const int i = find_item(hs->start, hs->tab.n, r);
-        if (!tab_bit(hs->bad, i)) {
-          const vitfe_item it = args.items[i];
-          int tg, hh, ww;
-          decode_local(r - hs->start[i], it.h, it.w, args.M, tg, hh, ww);
-          const int64_t H = (int64_t)it.h * P, W = (int64_t)it.w * P;
-          rs = W * 3;
-          const bool still = (it.frames == 1);
-          fstride = still ? 0 : H * W * 3;
-          const int64_t f0 = still ? 0 : (int64_t)tg * args.T;
-          base0 = args.pixels + it.pixel_offset + ((f0 * H + (int64_t)hh * P) * W + (int64_t)ww * P) * 3;
+    int tile = cid;
+    RowSrc cur = tile < args.num_tiles ? row_src<P>(args, hs, tile * kPairRows + rofs) : RowSrc{nullptr, 0, 0};
+    prefetch_row<P>(cur, args.T);
+    for (; ok && tile < args.num_tiles; tile += ncl) {
+      const int kind = tile_kind(tile * kPairRows, hs, args.T);
+      const int next = tile + ncl;
+      const RowSrc nxt = next < args.num_tiles ? row_src<P>(args, hs, next * kPairRows + rofs) : RowSrc{nullptr, 0, 0};
+      if (kind != kPad) {
+        const int nprod = (kind == kResident) ? 1 : args.npass * args.T;
+        for (int q = 0; ok && q < nprod; ++q) {
+          const int s = (kind == kResident) ? 0 : (q % args.T);
+          const uint8_t* base = cur.base0 ? cur.base0 + cur.fstride * s : nullptr;
+          ok = produce_slice<P>(base, cur.rs, a_smem, hs, np, row, sc, sh, abort_flag, args.limit_ns, a_full_L);
+          ++np;
+          if (q == 0) prefetch_row<P>(nxt, args.T);
         }
       }
-      const int nprod = (kind == kResident) ? 1 : args.npass * args.T;
-      for (int q = 0; ok && q < nprod; ++q) {
-        const int s = (kind == kResident) ? 0 : (q % args.T);
-        const uint8_t* base = base0 ? base0 + fstride * s : nullptr;
-        ok = produce_slice<P>(base, rs, a_smem, hs, np, row, sc, sh, abort_flag, args.limit_ns);
-        ++np;
-      }
+      cur = nxt;
     }
   } else if (warp == kTmaWarp) {
     if (lane == 0) {
-      uint32_t nb = 0;
+      uint32_t nb = 0, stage = 0, bphase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
-        const int kind = tile_kind(tile * kTileM, hs, args.T);
+      for (int tile = cid; ok && tile < args.num_tiles; tile += ncl) {
+        const int kind = tile_kind(tile * kPairRows, hs, args.T);
         if (kind == kPad) continue;
         for (int p = 0; ok && p < args.npass; ++p) {
           const int n0 = p * args.bn;
+          const int npw = min(args.bn, args.N - n0);
+          const int c1 = n0 + (int)rank * (npw / 2);
           const int nouter = (kind == kResident) ? NBLK : args.T;
           const int ninner = (kind == kResident) ? args.T : NBLK;
           for (int o = 0; ok && o < nouter; ++o) {
             for (int in = 0; ok && in < ninner; ++in) {
               const int j = (kind == kResident) ? o : in;
               const int s = (kind == kResident) ? in : o;
-              const uint32_t stage = nb % (uint32_t)args.nstage;
-              const uint32_t ph = (nb / (uint32_t)args.nstage) & 1u;
-              if (!mbar_wait(smem_u32(&hs->b_empty[stage]), ph ^ 1u, abort_flag, args.limit_ns)) {
+              if (!mbar_wait_cl(smem_u32(&hs->b_empty[stage]), bphase ^ 1u, abort_flag, args.limit_ns)) {
                 ok = false;
                 break;
               }
-              const uint32_t full = smem_u32(&hs->b_full[stage]);
-              mbar_arrive_expect_tx(full, b_stage_bytes);
-              tma_load_2d(b_smem + stage * b_stage_bytes, &tmap_w, full, s * args.kslice_pad + 64 * j, n0);
+              if (leader) mbar_arrive_expect_tx(smem_u32(&hs->b_full[stage]), 2u * b_stage_bytes);
+              tma_load_2d_pair(b_smem + stage * b_stage_bytes, &tmap_w, b_full_L + 8u * stage,
+                               s * args.kslice_pad + 64 * j, c1);
               ++nb;
+              if (++stage == (uint32_t)args.nstage) { stage = 0; bphase ^= 1u; }
             }
           }
         }
       }
       if (!ok) {
-        // drain: the last loads of every stage complete on their own
-        const uint32_t nlast = nb < (uint32_t)args.nstage ? nb : (uint32_t)args.nstage;
-        for (uint32_t d = 1; d <= nlast; ++d) {
-          const uint32_t idx = nb - d;
-          const uint32_t bar = smem_u32(&hs->b_full[idx % (uint32_t)args.nstage]);
-          const uint64_t t0 = global_timer_ns();
-          while (!mbar_try_wait(bar, (idx / (uint32_t)args.nstage) & 1u) &&
-                 global_timer_ns() - t0 < args.limit_ns) {
+        if (leader) {
+          // the last loads of every stage complete on their own
+          const uint32_t nlast = nb < (uint32_t)args.nstage ? nb : (uint32_t)args.nstage;
+          for (uint32_t d = 1; d <= nlast; ++d) {
+            const uint32_t idx = nb - d;
+            const uint32_t bar = smem_u32(&hs->b_full[idx % (uint32_t)args.nstage]);
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait_cluster(bar, (idx / (uint32_t)args.nstage) & 1u) &&
+                   global_timer_ns() - t0 < args.limit_ns) {
+            }
           }
+        } else {
+          // this CTA's copies signal the even CTA's barriers: give them time to land
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 200000ull) __nanosleep(1000);
         }
       }
     }
   } else if (warp == kMmaWarp) {
-    if (lane == 0) {
-      uint32_t nb = 0, na = 0, np = 0;
+    if (lane == 0 && leader) {
+      // The tensor core queues few MMAs: everything this thread does between MMA
+      // issues is kept to a minimum (precomputed descriptors, CTA-scope waits on the
+      // TMA barriers, unrolled K blocks).
+      uint32_t na = 0, np = 0, stage = 0, bphase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
-        const int kind = tile_kind(tile * kTileM, hs, args.T);
+      const uint64_t adesc0 = sw128_desc(a_smem);
+      const uint64_t bdesc0 = sw128_desc(b_smem);
+      const uint64_t bstage_desc = (uint64_t)(b_stage_bytes >> 4);
+      auto b_step = [&](uint64_t adesc, int nk, uint32_t d_tmem, uint32_t idesc, uint32_t& accum) -> bool {
+        if (!mbar_wait(smem_u32(&hs->b_full[stage]), bphase, abort_flag, args.limit_ns)) return false;
+        const uint64_t bdesc = bdesc0 + bstage_desc * stage;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          if (kk < nk) {
+            umma_bf16_pair(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc, accum);
+            accum = 1;
+          }
+        }
+        umma_commit_pair(smem_u32(&hs->b_empty[stage]));
+        if (++stage == (uint32_t)args.nstage) { stage = 0; bphase ^= 1u; }
+        return true;
+      };
+      for (int tile = cid; ok && tile < args.num_tiles; tile += ncl) {
+        const int kind = tile_kind(tile * kPairRows, hs, args.T);
         if (kind == kPad) continue;
         for (int p = 0; ok && p < args.npass; ++p) {
           const uint32_t buf = na & 1u;
-          if (!mbar_wait(smem_u32(&hs->acc_empty[buf]), ((na >> 1) & 1u) ^ 1u, abort_flag, args.limit_ns)) {
+          if (!mbar_wait_cl(smem_u32(&hs->acc_empty[buf]), ((na >> 1) & 1u) ^ 1u, abort_flag, args.limit_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const int npw = min(args.bn, args.N - p * args.bn);
-          const uint32_t idesc = idesc_bf16(kTileM, npw);
+          const uint32_t idesc = idesc_bf16(kPairRows, npw);
           const uint32_t d_tmem = tmem + buf * (uint32_t)args.bn;
           uint32_t accum = 0;
-          const int nouter = (kind == kResident) ? NBLK : args.T;
-          const int ninner = (kind == kResident) ? args.T : NBLK;
-          for (int o = 0; ok && o < nouter; ++o) {
-            for (int in = 0; ok && in < ninner; ++in) {
-              const int j = (kind == kResident) ? o : in;
-              const bool first_use = (kind == kResident) ? (p == 0 && in == 0) : true;
-              const bool last_use = (kind == kResident) ? (p == args.npass - 1 && in == ninner - 1) : true;
-              if (first_use) {
-                if (!mbar_wait(smem_u32(&hs->a_full[j]), np & 1u, abort_flag, args.limit_ns)) {
+          if (kind == kResident) {
+            // one resident slice of A feeds every temporal slice of W
+#pragma unroll
+            for (int j = 0; j < NBLK; ++j) {
+              if (p == 0) {
+                if (!mbar_wait_cl(smem_u32(&hs->a_full[j]), np & 1u, abort_flag, args.limit_ns)) { ok = false; break; }
+                tc_fence_after();
+              }
+              const uint64_t adesc = adesc0 + (uint64_t)(j * (kABlockBytes >> 4));
+              for (int s = 0; s < args.T; ++s)
+                if (!b_step(adesc, ksteps_of<P>(j), d_tmem, idesc, accum)) { ok = false; break; }
+              if (!ok) break;
+              if (p == args.npass - 1) umma_commit_pair(smem_u32(&hs->a_empty[j]));
+            }
+          } else {
+            for (int s = 0; ok && s < args.T; ++s) {
+#pragma unroll
+              for (int j = 0; j < NBLK; ++j) {
+                if (!mbar_wait_cl(smem_u32(&hs->a_full[j]), np & 1u, abort_flag, args.limit_ns)) { ok = false; break; }
+                tc_fence_after();
+                if (!b_step(adesc0 + (uint64_t)(j * (kABlockBytes >> 4)), ksteps_of<P>(j), d_tmem, idesc, accum)) {
                   ok = false;
                   break;
                 }
+                umma_commit_pair(smem_u32(&hs->a_empty[j]));
               }
-              const uint32_t stage = nb % (uint32_t)args.nstage;
-              if (!mbar_wait(smem_u32(&hs->b_full[stage]), (nb / (uint32_t)args.nstage) & 1u, abort_flag,
-                             args.limit_ns)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint32_t a_addr = a_smem + (uint32_t)j * kABlockBytes;
-              const uint32_t b_addr = b_smem + stage * b_stage_bytes;
-              const int nk = ksteps_of<P>(j);
-              for (int kk = 0; kk < nk; ++kk) {
-                umma_bf16(d_tmem, sw128_desc(a_addr + 32u * kk), sw128_desc(b_addr + 32u * kk), idesc, accum);
-                accum = 1;
-              }
-              umma_commit(smem_u32(&hs->b_empty[stage]));
-              ++nb;
-              if (last_use) umma_commit(smem_u32(&hs->a_empty[j]));
+              ++np;   // one slice production consumed
             }
-            if (kind == kStream) ++np;   // one slice production consumed per outer step
           }
           if (!ok) break;
-          umma_commit(smem_u32(&hs->acc_full[buf]));
+          umma_commit_pair(smem_u32(&hs->acc_full[buf]));
           ++na;
         }
         if (kind == kResident) ++np;
       }
       if (!ok) {
-        umma_commit(smem_u32(&hs->drain));
+        umma_commit_pair(smem_u32(&hs->drain));
         const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(smem_u32(&hs->drain), 0u) && global_timer_ns() - t0 < args.limit_ns) {
+        while (!mbar_try_wait_cluster(smem_u32(&hs->drain), 0u) && global_timer_ns() - t0 < args.limit_ns) {
         }
       }
     }
   } else {
-    // epilogue warps 4..7: TMEM lanes 32*(warp%4) .. +31
+    // epilogue warps 4..11: lane quarter q = warp % 4 of this CTA's accumulator rows,
+    // column half h of every pass
     const int q = warp & 3;
-    const int rloc = q * 32 + lane;
+    const int h = (warp - 4) >> 2;
+    const int rloc = (int)rank * kTileM + q * 32 + lane;
+    const bool out32 = (reinterpret_cast<uintptr_t>(args.out) & 31u) == 0;
     uint32_t na = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
-      const int r0 = tile * kTileM;
+    for (int tile = cid; ok && tile < args.num_tiles; tile += ncl) {
+      const int r0 = tile * kPairRows;
       const int kind = tile_kind(r0, hs, args.T);
       const int r = r0 + rloc;
       const bool in_bucket = r < args.rows;
@@ -394,40 +489,56 @@ __global__ void __launch_bounds__(kThreads, 1) embed_kernel(const __grid_constan
       if (kind == kPad) {
         if (in_bucket) {
           const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-          for (int c = 0; c < args.N; c += 8) *reinterpret_cast<uint4*>(orow + c) = z;
+          const int half = args.N / 2;
+          for (int c = h * half; c < (h + 1) * half; c += 8) *reinterpret_cast<uint4*>(orow + c) = z;
         }
         continue;
       }
       for (int p = 0; p < args.npass; ++p) {
         const uint32_t buf = na & 1u;
-        if (!mbar_wait(smem_u32(&hs->acc_full[buf]), (na >> 1) & 1u, abort_flag, args.limit_ns)) {
+        if (!mbar_wait_cl(smem_u32(&hs->acc_full[buf]), (na >> 1) & 1u, abort_flag, args.limit_ns, 64)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const int npw = min(args.bn, args.N - p * args.bn);
-        for (int c0 = 0; c0 < npw; c0 += 32) {
+        const int cw = npw / 2;     // columns of this warp (a multiple of 16)
+        for (int c0 = h * cw; c0 < (h + 1) * cw; c0 += 32) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + buf * (uint32_t)args.bn + (uint32_t)c0, v);
           tmem_wait_ld();
+          const int ncol = min(32, (h + 1) * cw - c0);   // 32, or 16 for a 16-column tail
           if (in_bucket) {
             const int n0 = p * args.bn + c0;
             uint32_t pk[16];
+            const float4* bias4 = reinterpret_cast<const float4*>(args.bias + n0);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float y0 = __uint_as_float(v[2 * e]) + __ldg(args.bias + n0 + 2 * e);
-              const float y1 = __uint_as_float(v[2 * e + 1]) + __ldg(args.bias + n0 + 2 * e + 1);
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(y0, y1);
-              pk[e] = valid ? *reinterpret_cast<uint32_t*>(&b2) : 0u;
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const float4 bv = e4 * 4 < ncol ? __ldg(bias4 + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+              __nv_bfloat162 b0 = __floats2bfloat162_rn(__uint_as_float(v[4 * e4]) + bv.x,
+                                                        __uint_as_float(v[4 * e4 + 1]) + bv.y);
+              __nv_bfloat162 b1 = __floats2bfloat162_rn(__uint_as_float(v[4 * e4 + 2]) + bv.z,
+                                                        __uint_as_float(v[4 * e4 + 3]) + bv.w);
+              pk[2 * e4] = valid ? *reinterpret_cast<uint32_t*>(&b0) : 0u;
+              pk[2 * e4 + 1] = valid ? *reinterpret_cast<uint32_t*>(&b1) : 0u;
             }
-            uint4* dst = reinterpret_cast<uint4*>(orow + n0);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              __stcs(dst + e, make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]));
+            __nv_bfloat16* dst = orow + n0;
+            if (out32) {
+              st_global_v8(dst, pk);
+              if (ncol == 32) st_global_v8(dst + 16, pk + 8);
+            } else {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+              __stcs(d4, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+              __stcs(d4 + 1, make_uint4(pk[4], pk[5], pk[6], pk[7]));
+              if (ncol == 32) {
+                __stcs(d4 + 2, make_uint4(pk[8], pk[9], pk[10], pk[11]));
+                __stcs(d4 + 3, make_uint4(pk[12], pk[13], pk[14], pk[15]));
+              }
+            }
           }
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&hs->acc_empty[buf]));
+        mbar_arrive_cluster(acc_empty_L + 8u * buf);
         ++na;
       }
     }
@@ -436,9 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1) embed_kernel(const __grid_constan
   // ---- teardown ------------------------------------------------------------
   __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, (uint32_t)args.tmem_cols);
+  if (warp == kMmaWarp) tmem_dealloc_pair(tmem, (uint32_t)args.tmem_cols);
   if (threadIdx.x == 0 && hs->abort_flag && args.status != nullptr) {
     args.status[0] = kTimeout;
     args.status[1] = -1;
@@ -453,29 +564,43 @@ size_t embed_smem_bytes(int nblk, int bn, int nstage) {
 
 cudaError_t embed_configure(Ctx& c) {
   c.embed_ok = false;
-  // implemented: patch 14 or 16 (Qwen2/2.5-VL and Qwen3-VL); hidden a multiple of 32
-  if (!(c.P == 14 || c.P == 16) || (c.N % 32) != 0) return cudaSuccess;
+  // implemented: patch 14 or 16 (Qwen2/2.5-VL and Qwen3-VL); hidden a multiple of 64
+  // (each epilogue warp stores whole 32-column groups of its half of a pass)
+  if (!(c.P == 14 || c.P == 16) || (c.N % 64) != 0) return cudaSuccess;
   int max_optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
   if (e != cudaSuccess) return e;
-  const int cand[][2] = {{256, 2}, {128, 3}, {128, 2}};
-  for (auto& cb : cand) {
-    const int bn = cb[0] > c.N ? c.N : cb[0];
-    const size_t need = embed_smem_bytes(c.nblk, bn, cb[1]);
+  const int bn = c.N < 256 ? c.N : 256;
+  for (int nst = 8; nst >= 2; --nst) {
+    const size_t need = embed_smem_bytes(c.nblk, bn / 2, nst);
     if (need <= (size_t)max_optin) {
       c.bn = bn;
-      c.nstage = cb[1];
+      c.nstage = nst;
       c.embed_smem = need;
       c.embed_ok = true;
       break;
     }
   }
   if (!c.embed_ok) return cudaSuccess;
-  if (c.P == 14)
-    e = cudaFuncSetAttribute(embed_kernel<14>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.embed_smem);
-  else
-    e = cudaFuncSetAttribute(embed_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.embed_smem);
-  return e;
+  const void* fn = (c.P == 14) ? (const void*)embed_kernel<14> : (const void*)embed_kernel<16>;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.embed_smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (c.sm_count / 2), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = c.embed_smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int ncl = 0;
+  e = cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg);
+  if (e != cudaSuccess) return e;
+  c.max_clusters = ncl > 0 ? ncl : 1;
+  return cudaSuccess;
 }
 
 cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_bytes,
@@ -502,10 +627,11 @@ cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_byte
   a.npass = (c.N + c.bn - 1) / c.bn;
   a.tmem_cols = 32;
   while (a.tmem_cols < 2 * c.bn) a.tmem_cols <<= 1;
-  a.num_tiles = (int)((rows + kTileM - 1) / kTileM);
+  a.num_tiles = (int)((rows + kPairRows - 1) / kPairRows);
   a.limit_ns = c.wait_limit_ns;
-  int grid = a.num_tiles < c.sm_count ? a.num_tiles : c.sm_count;
-  if (grid < 1) grid = 1;
+  int pairs = a.num_tiles < c.max_clusters ? a.num_tiles : c.max_clusters;
+  if (pairs < 1) pairs = 1;
+  const int grid = 2 * pairs;
   if (c.P == 14)
     embed_kernel<14><<<grid, kThreads, c.embed_smem, s>>>(c.tmap_w, a);
   else

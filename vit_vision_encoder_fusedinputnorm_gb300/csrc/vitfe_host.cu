@@ -136,7 +136,8 @@ vitfe_status vitfe_create(vitfe_t* out, const float mean[3], const float std_[3]
     }
     const cuuint64_t gdim[2] = {(cuuint64_t)c.kint, (cuuint64_t)c.N};
     const cuuint64_t gstride[1] = {(cuuint64_t)c.kint * sizeof(__nv_bfloat16)};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)c.bn};
+    // each CTA of a pair loads half of a tile's W rows
+    const cuuint32_t box[2] = {64u, (cuuint32_t)(c.bn / 2)};
     const cuuint32_t estride[2] = {1u, 1u};
     CUresult r = enc(&c.tmap_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.w_int, gdim, gstride, box, estride,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
