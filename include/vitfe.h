@@ -130,6 +130,24 @@ vitfe_status vitfe_pos_ids(vitfe_t h, const vitfe_item* items, const int32_t* n_
                            int32_t max_items, int64_t rows, int32_t* pos, int32_t* status,
                            cudaStream_t stream);
 
+/* Allocation-free 2D-RoPE tables, for callers that cannot allocate device memory:
+ * code under a memory pool it does not own, inside a CUDA-graph capture that must
+ * not allocate, or in a process that may not call cudaMalloc after start-up.  No
+ * counterpart in the pages; it computes exactly what vitfe_rope computes, without a
+ * handle (tpatch and merge are passed directly).
+ * Scratch: a 1 MiB file-scope device array that every GPU loading the library
+ * keeps until exit; it bounds head_dim to 128 (VITFE_EUNSUPPORTED above that, up
+ * to VITFE_ROPE_MAX_HEAD_DIM) and h, w to VITFE_ROPE_MAX_SIDE (checked on the
+ * device, VITFE_EDEVICE_DESC).  The call allocates and frees nothing.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All calls
+ * share the array: calls that overlap on the GPU (other streams, other threads)
+ * race and must be ordered by the caller.  Arguments, layouts and errors are
+ * otherwise those of vitfe_rope. */
+vitfe_status vitfe_rope_noalloc(int tpatch, int merge, const vitfe_item* items, const int32_t* n_items,
+                                int32_t max_items, int64_t rows, int head_dim, float theta,
+                                float* cos, float* sin, int32_t* status, cudaStream_t stream);
+
 /* Host helper: build packed item descriptors from grid_thw.
  * grid_thw (host int32 [n][3]); is_still (host uint8 [n], nonzero = a still
  * stored as one frame; NULL = every item with t == 1 is a still).

@@ -94,3 +94,13 @@ def test_calls_reject_null_handle(lib):
         with pytest.raises(B.VitfeError) as e:
             fn(*args)
         assert e.value.code == 1
+
+
+def test_noalloc_rope_rejects_sizes_beyond_its_static_table(lib):
+    # head_dim above 128 does not fit the fixed scratch table: a clear error, nothing launched
+    with pytest.raises(B.VitfeError) as e:
+        B.vitfe_rope_noalloc(2, 2, 16, 16, 1, 10, 256, 1e4, 16, 16)
+    assert e.value.code == 7
+    with pytest.raises(B.VitfeError) as e:
+        B.vitfe_rope_noalloc(2, 2, 16, 16, 1, 10, 84, 1e4, 16, 16)      # not a multiple of 8
+    assert e.value.code == 1

@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "VITFE_OK", 1: "VITFE_EINVAL", 2: "VITFE_ENOMEM", 3: "VITFE_E
 
 # exported symbols of include/vitfe.h
 EXPORTS = ["vitfe_create", "vitfe_destroy", "vitfe_embed", "vitfe_rope", "vitfe_normalize_patchify",
-           "vitfe_pos_ids", "vitfe_items_from_grid", "vitfe_feature_dim", "vitfe_status_str"]
+           "vitfe_pos_ids", "vitfe_rope_noalloc", "vitfe_items_from_grid", "vitfe_feature_dim",
+           "vitfe_status_str"]
 
 ITEM_DTYPE = np.dtype([("pixel_offset", "<i8"), ("t", "<i4"), ("h", "<i4"), ("w", "<i4"),
                        ("frames", "<i4")])
@@ -64,6 +65,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.vitfe_embed.restype = ctypes.c_int
     lib.vitfe_rope.argtypes = [P, P, P, I32, I64, ctypes.c_int, F32, P, P, P, P]
     lib.vitfe_rope.restype = ctypes.c_int
+    lib.vitfe_rope_noalloc.argtypes = [ctypes.c_int, ctypes.c_int, P, P, I32, I64, ctypes.c_int, F32, P, P, P, P]
+    lib.vitfe_rope_noalloc.restype = ctypes.c_int
     lib.vitfe_normalize_patchify.argtypes = [P, P, I64, P, P, I32, I64, P, P, P]
     lib.vitfe_normalize_patchify.restype = ctypes.c_int
     lib.vitfe_pos_ids.argtypes = [P, P, P, I32, I64, P, P, P]
@@ -130,6 +133,14 @@ def vitfe_rope(h, items, n_items, max_items, rows, head_dim, theta, cos, sin, st
     _check("vitfe_rope", load().vitfe_rope(h, _ptr(items), _ptr(n_items), int(max_items), int(rows),
                                            int(head_dim), float(theta), _ptr(cos), _ptr(sin), _ptr(status),
                                            _stream(stream)))
+
+
+def vitfe_rope_noalloc(tpatch, merge, items, n_items, max_items, rows, head_dim, theta, cos, sin, status=None,
+                       stream=None) -> None:
+    _check("vitfe_rope_noalloc", load().vitfe_rope_noalloc(int(tpatch), int(merge), _ptr(items), _ptr(n_items),
+                                                           int(max_items), int(rows), int(head_dim),
+                                                           float(theta), _ptr(cos), _ptr(sin), _ptr(status),
+                                                           _stream(stream)))
 
 
 def vitfe_normalize_patchify(h, pixels, pixel_bytes, items, n_items, max_items, rows, out, status=None,

@@ -1,5 +1,8 @@
 // Side paths of the front end (sm_103a): position ids, 2D-RoPE tables, standalone
 // FusedInputNorm + patchify, and the create-time weight permutation.
+#include <cmath>
+#include <mutex>
+
 #include "vitfe_internal.cuh"
 
 namespace vitfe {
@@ -392,3 +395,84 @@ cudaError_t launch_permute_weight(const Ctx& c, const __nv_bfloat16* W, const __
 }
 
 }  // namespace vitfe
+
+// ---------------------------------------------------------------------------
+// Allocation-free RoPE entry point.
+//
+// Some callers cannot allocate device memory at all: code running under an
+// allocator they do not own (a serving runtime whose memory pool is carved up in
+// advance, or a CUDA-graph capture that must not allocate), or a host process
+// that is forbidden to call cudaMalloc after start-up.  vitfe_rope needs a handle,
+// and creating one allocates.  vitfe_rope_noalloc runs the same two RoPE kernels
+// with their axis-table scratch in the file-scope array below instead: 1 MiB,
+// enough for position tables up to VITFE_ROPE_MAX_SIDE positions and head_dim up
+// to 128.  Every GPU that loads this library holds the array until the process
+// exits.
+// ---------------------------------------------------------------------------
+namespace vitfe {
+namespace {
+
+constexpr int kStaticRopeMaxHeadDim = 128;
+constexpr size_t kStaticRopeFloats = (size_t)2 * VITFE_ROPE_MAX_SIDE * (kStaticRopeMaxHeadDim / 4);
+
+// Host code must never pass this symbol to a kernel: on the host it names a
+// shadow variable, not device memory.  Its device address comes from
+// cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) float g_rope_scratch[kStaticRopeFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+float* g_scratch_ptr[kMaxDevices] = {};
+int g_scratch_sms[kMaxDevices] = {};
+
+// Looks up (once per device, with that device current) the device address of the
+// scratch array and the SM count.
+cudaError_t static_scratch(int dev, float** ptr, int* sms) {
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_rope_scratch);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_scratch_sms[dev] = n;
+    g_scratch_ptr[dev] = static_cast<float*>(p);
+  }
+  *ptr = g_scratch_ptr[dev];
+  *sms = g_scratch_sms[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace vitfe
+
+extern "C" vitfe_status vitfe_rope_noalloc(int tpatch, int merge, const vitfe_item* items,
+                                           const int32_t* n_items, int32_t max_items, int64_t rows,
+                                           int head_dim, float theta, float* cos, float* sin,
+                                           int32_t* status, cudaStream_t stream) {
+  if (items == nullptr || n_items == nullptr) return VITFE_EINVAL;
+  if (tpatch < 1 || tpatch > 4 || merge < 1 || merge > 8) return VITFE_EINVAL;
+  if (max_items < 0 || max_items > VITFE_MAX_ITEMS) return VITFE_EINVAL;
+  if (rows < 0 || rows > 0x7fffffffLL - 1024) return VITFE_EINVAL;
+  if (head_dim < 8 || (head_dim % 8) != 0 || head_dim > VITFE_ROPE_MAX_HEAD_DIM) return VITFE_EINVAL;
+  if (head_dim > vitfe::kStaticRopeMaxHeadDim) return VITFE_EUNSUPPORTED;   // beyond the static scratch
+  if (!std::isfinite(theta) || !(theta > 0.0f)) return VITFE_EINVAL;
+  if (rows > 0 && (cos == nullptr || sin == nullptr)) return VITFE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(cos) & 15u) || (reinterpret_cast<uintptr_t>(sin) & 15u)) return VITFE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(items) & 7u) || (reinterpret_cast<uintptr_t>(n_items) & 3u)) return VITFE_EINVAL;
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return VITFE_EINVAL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= vitfe::kMaxDevices) return VITFE_ECUDA;
+  float* tab = nullptr;
+  int sms = 0;
+  if (vitfe::static_scratch(dev, &tab, &sms) != cudaSuccess) return VITFE_ECUDA;
+  const int nf = head_dim / 4;
+  vitfe::rope_table_kernel<<<32, vitfe::kAuxThreads, 0, stream>>>(items, n_items, max_items, tpatch, merge,
+                                                                  (int)rows, nf, (double)theta, tab);
+  if (cudaGetLastError() != cudaSuccess) return VITFE_ECUDA;
+  const int grid = vitfe::grid_for(rows, vitfe::kAuxThreads, sms * 16);
+  vitfe::rope_expand_kernel<<<grid, vitfe::kAuxThreads, 0, stream>>>(items, n_items, max_items, tpatch, merge,
+                                                                     (int)rows, nf, tab, cos, sin, status);
+  return cudaGetLastError() == cudaSuccess ? VITFE_OK : VITFE_ECUDA;
+}
