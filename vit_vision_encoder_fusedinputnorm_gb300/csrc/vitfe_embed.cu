@@ -9,14 +9,15 @@
 // Structure: persistent clusters of two CTAs (one per SM).  A pair owns 256-row tiles,
 // 128 rows per CTA; one tcgen05.mma.cta_group::2 (M=256) spans both CTAs' shared and
 // tensor memory, so each CTA holds only half of every W tile.  Per CTA, 14 warps:
-//   warps 0-3   A producers: one thread per tile row gathers uint8 pixel runs with
-//               aligned 4-byte loads, normalises in fp32, rounds to bf16 and stores
-//               into 128-byte-swizzled K-major shared-memory blocks (64 features each);
+//   warps 0-7   A producers: two threads per tile row (each half of the K blocks) gather
+//               uint8 pixel runs with aligned 4-byte loads, normalise in fp32, round to
+//               bf16 and store into 128-byte-swizzled K-major shared-memory blocks (64
+//               features each);
 //   warp 12     TMA producer of this CTA's half of each W tile (box 64 x bn/2);
 //   warp 13     tensor-memory allocation (both CTAs); in the even CTA one thread issues
 //               the MMAs (fp32 accumulators double-buffered in tensor memory);
-//   warps 4-11  epilogue, two warps per tensor-memory lane quarter (each half of the
-//               columns): tcgen05.ld of the accumulator, + bias, bf16 RNE, 256-bit stores.
+//   warps 8-11  epilogue, one warp per tensor-memory lane quarter: tcgen05.ld of the
+//               accumulator, + bias, bf16 RNE, 256-bit stores.
 // Barriers that gather both CTAs (A ready, W tile ready, accumulator free) live in the
 // even CTA; the MMA's completion is multicast to both CTAs.
 //
@@ -35,8 +36,10 @@ namespace vitfe {
 namespace {
 
 constexpr int kThreads = 448;
-constexpr int kProducerThreads = 128;
-constexpr int kEpilogueThreads = 256;     // two warps per tensor-memory lane quarter
+constexpr int kProducerThreads = 128;     // tile rows of a CTA (two producer threads each)
+constexpr int kProducerWarps = 8;
+constexpr int kEpilogueWarp0 = 8;
+constexpr int kEpilogueThreads = 128;     // one warp per tensor-memory lane quarter
 constexpr int kPairRows = 2 * kTileM;
 constexpr int kTmaWarp = 12;
 constexpr int kMmaWarp = 13;
@@ -101,100 +104,163 @@ __host__ __device__ constexpr int ksteps_of(int j) {
   return rem >= 64 ? 4 : (rem + 15) / 16;
 }
 
-// One A producer thread writes its row of one temporal slice (all K blocks, in order).
-// base: first byte of the patch (top-left pixel, channel 0) in the slice's frame, or
-// nullptr for rows written as zeros.  rs: bytes between pixel rows.
-template <int P>
-__device__ __forceinline__ bool produce_slice(const uint8_t* base, int64_t rs, uint32_t a_smem,
-                                              SmemHdr* hs, uint32_t np, int row, const float sc[3],
-                                              const float sh[3], volatile int* abort_flag,
-                                              uint64_t limit_ns, uint32_t a_full_leader) {
+// Two fp32 lanes in one 64-bit register (packed f32x2 arithmetic, exact per lane).
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, uint32_t& lo, uint32_t& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+// x = (v - 2^23) * scale + shift on both lanes; v holds 2^23 + byte (exact).
+__device__ __forceinline__ uint64_t norm2(uint64_t v, uint64_t scale2, uint64_t shift2) {
+  const uint64_t m = 0xCB000000CB000000ull;   // (-2^23, -2^23)
+  uint64_t t, x;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(t) : "l"(v), "l"(m));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(x) : "l"(t), "l"(scale2), "l"(shift2));
+  return x;
+}
+
+// One A producer thread writes K blocks [JB, JE) of its row of one temporal slice, in
+// order.  base: first byte of the patch (top-left pixel, channel 0) in the slice's frame,
+// or nullptr for rows written as zeros.  rs: bytes between pixel rows.  Two threads share
+// a row (one per half of the K blocks), so that two producer warps per SM sub-partition
+// hide each other's load latency.
+//
+// Schedule per K block j: convert and store its 64 features, make them visible to the
+// tensor core (proxy fence + release arrive on the even CTA's barrier), then issue the
+// loads of the patch rows that start in block j+1 and wait for block j+1's shared-memory
+// slot to be freed.  Every load is consumed inside the block it starts in, so no load is
+// in flight when the release arrive executes (a release waits for the thread's pending
+// loads); the load latency overlaps the wait for the free slot.
+template <int P, int JB, int JE>
+__device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, uint32_t a_smem,
+                                               SmemHdr* hs, uint32_t np, int row, const float sc[3],
+                                               const float sh[3], volatile int* abort_flag,
+                                               uint64_t limit_ns, uint32_t a_full_leader) {
   constexpr int RUN = 3 * P;                 // bytes of one patch row of pixels
   constexpr int KS = 3 * P * P;
   constexpr int NBLK = (KS + 63) / 64;
   constexpr int KEND = ((KS + 15) / 16) * 16;  // features written (K16 padded)
   constexpr int NW = (RUN + 3) / 4 + 1;      // 4-byte words covering a run at any alignment
   constexpr int NA = (RUN + 3) / 4;          // aligned words holding the run
-  static_assert(RUN % 2 == 0, "patch rows must hold an even number of bytes");
+  constexpr int E0 = 64 * JB;                // first feature of the range
+  constexpr int E1 = (64 * JE < KEND) ? 64 * JE : KEND;   // one past the last feature written
+  constexpr int R0 = E0 / RUN;               // first pixel row touched
+  constexpr int RL = ((E1 < KS ? E1 : KS) - 1) / RUN;      // last pixel row touched
+  // Register ring of loaded pixel rows: row r+2 is loaded at the end of a block that
+  // comes after row r started (2*RUN > 64), so two slots suffice -- except at the start of
+  // a range that begins inside row R0, where row R0+2 may also start in block JB: its load
+  // is deferred until row R0 has been aligned (DEFER).
+  constexpr int R = 2;
+  constexpr bool CARRY = (R0 * RUN < E0) && R0 < P;            // R0 started before the range
+  constexpr bool DEFER = CARRY && (R0 + 2 < P) && ((R0 + 2) * RUN < 64 * (JB + 1));
+  static_assert(RUN % 2 == 0 && RUN > 32, "patch rows: even length, at most two start per block");
+  static_assert(NBLK <= 16 && JB < JE && JE <= NBLK, "A slots");
+  // (scale, shift) of the channel pairs (c, c+1 mod 3) that a feature pair starting at
+  // channel c covers
+  const uint64_t sc2[3] = {pack2(__float_as_uint(sc[0]), __float_as_uint(sc[1])),
+                           pack2(__float_as_uint(sc[1]), __float_as_uint(sc[2])),
+                           pack2(__float_as_uint(sc[2]), __float_as_uint(sc[0]))};
+  const uint64_t sh2[3] = {pack2(__float_as_uint(sh[0]), __float_as_uint(sh[1])),
+                           pack2(__float_as_uint(sh[1]), __float_as_uint(sh[2])),
+                           pack2(__float_as_uint(sh[2]), __float_as_uint(sh[0]))};
   const uint32_t empty_parity = (np & 1u) ^ 1u;
   const uint32_t row_off = (uint32_t)row * 128u;
   const uint32_t swz = (uint32_t)(row & 7);
   uint32_t cw[4] = {0u, 0u, 0u, 0u};         // bf16x2 words of the chunk being assembled
+  uint32_t raw[R][NW];
+  const uint32_t a_empty0 = smem_u32(&hs->a_empty[0]);
 
-  auto emit_word = [&](int kw, uint32_t word) -> bool {
-    // kw: index of the bf16 pair inside the slice
-    cw[kw & 3] = word;
-    if ((kw & 3) == 3) {
-      const int kc = kw >> 2;          // chunk of 8 features
-      const int j = kc >> 3;           // K block
-      const int q = kc & 7;            // chunk inside the 128-byte row
-      if (q == 0) {
-        if (!mbar_wait_cl(smem_u32(&hs->a_empty[j]), empty_parity, abort_flag, limit_ns, 128)) return false;
-      }
-      const uint32_t addr = a_smem + (uint32_t)j * kABlockBytes + row_off + (((uint32_t)q ^ swz) << 4);
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(cw[0]), "r"(cw[1]),
-                   "r"(cw[2]), "r"(cw[3])
-                   : "memory");
-      const bool last_of_block = (q == 7) || (kc == KEND / 8 - 1);
-      if (last_of_block) {
-        fence_proxy_async_all();
-        mbar_arrive_cluster(a_full_leader + 8u * (uint32_t)j);
-      }
-    }
-    return true;
-  };
+#define VITFE_LOAD_ROW(PH)                                                                  \
+  do {                                                                                       \
+    if (base != nullptr) {                                                                   \
+      const uintptr_t a_ = reinterpret_cast<uintptr_t>(base + (int64_t)(PH) * rs);          \
+      const uint32_t s_ = (uint32_t)(a_ & 3u);                                               \
+      const uint32_t* w0_ = reinterpret_cast<const uint32_t*>(a_ & ~uintptr_t(3));           \
+      _Pragma("unroll") for (int w_ = 0; w_ < NW; ++w_)                                     \
+        raw[(PH) % R][w_] = (4u * w_ < s_ + RUN) ? __ldg(w0_ + w_) : 0u;                     \
+    }                                                                                        \
+  } while (0)
+  // Rows starting in block b: [ceil(64b/RUN), ceil(64(b+1)/RUN)); at most two.
+#define VITFE_ROWS_OF_BLOCK(B)                                                    \
+  do {                                                                             \
+    const int lo_ = (64 * (B) + RUN - 1) / RUN;                                    \
+    const int hi_ = (64 * ((B) + 1) + RUN - 1) / RUN;                              \
+    if (lo_ < hi_ && lo_ < P) VITFE_LOAD_ROW(lo_);                                 \
+    if (lo_ + 1 < hi_ && lo_ + 1 < P) VITFE_LOAD_ROW(lo_ + 1);                     \
+  } while (0)
 
-  // Loads of patch row ph+1 are issued before row ph is converted and stored, so the
-  // global-load latency overlaps the conversion instead of adding up over the P rows.
-  uint32_t raw[2][NW];
-  auto load_run = [&](int ph, uint32_t (&dst)[NW]) {
-    if (base != nullptr) {
-      const uintptr_t a = reinterpret_cast<uintptr_t>(base + (int64_t)ph * rs);
-      const uint32_t s = (uint32_t)(a & 3u);
-      const uint32_t* w0 = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+  // first block: the row it starts inside (if a row began in an earlier block), the rows
+  // that start in it, then its slot
+  if (CARRY) VITFE_LOAD_ROW(R0);
+  {
+    const int lo_ = (64 * JB + RUN - 1) / RUN;
+    const int hi_ = (64 * (JB + 1) + RUN - 1) / RUN;
+    if (lo_ < hi_ && lo_ < P && !(DEFER && lo_ == R0 + 2)) VITFE_LOAD_ROW(lo_);
+    if (lo_ + 1 < hi_ && lo_ + 1 < P && !(DEFER && lo_ + 1 == R0 + 2)) VITFE_LOAD_ROW(lo_ + 1);
+  }
+  if (!mbar_wait_cl(a_empty0 + 8u * JB, empty_parity, abort_flag, limit_ns, 128)) return false;
+
 #pragma unroll
-      for (int w = 0; w < NW; ++w) dst[w] = (4u * w < s + RUN) ? __ldg(w0 + w) : 0u;
-    }
-  };
-  const uint32_t sel = base ? 0x3210u + 0x1111u * (uint32_t)(reinterpret_cast<uintptr_t>(base) & 3u) : 0x3210u;
-  // all runs of a patch share the byte alignment only when rs is a multiple of 4; otherwise
-  // the selector is recomputed per row
-  const bool same_align = (rs & 3) == 0;
-  load_run(0, raw[0]);
-#pragma unroll
-  for (int ph = 0; ph < P; ++ph) {
-    if (ph + 1 < P) load_run(ph + 1, raw[(ph + 1) & 1]);
+  for (int ph = R0; ph <= P; ++ph) {
+    // ph == P: the zero features [KS, KEND) of the last K16 step
+    if (ph > RL && ph < P) continue;
+    if (ph == P && E1 <= KS) continue;
     uint32_t al[NA];
-    if (base != nullptr) {
-      const uint32_t sl = same_align ? sel
-          : 0x3210u + 0x1111u * (uint32_t)(reinterpret_cast<uintptr_t>(base + (int64_t)ph * rs) & 3u);
+    if (ph < P && base != nullptr) {
+      const uint32_t sl = 0x3210u + 0x1111u * (uint32_t)(reinterpret_cast<uintptr_t>(base + (int64_t)ph * rs) & 3u);
 #pragma unroll
-      for (int w = 0; w < NA; ++w) al[w] = __byte_perm(raw[ph & 1][w], raw[ph & 1][w + 1], sl);
+      for (int w = 0; w < NA; ++w) al[w] = __byte_perm(raw[ph % R][w], raw[ph % R][w + 1], sl);
+      if (DEFER && ph == R0) VITFE_LOAD_ROW(R0 + 2);
     } else {
 #pragma unroll
       for (int w = 0; w < NA; ++w) al[w] = 0u;
     }
+    const int row_start = (ph < P) ? ph * RUN : KS;
+    const int row_end = (ph < P) ? (ph + 1) * RUN : KEND;
+    const int e_lo = (row_start < E0 ? E0 : row_start) - row_start;
+    const int e_hi = (row_end > E1 ? E1 : row_end) - row_start;
 #pragma unroll
     for (int e = 0; e < RUN; e += 2) {
+      if (e < e_lo || e >= e_hi) continue;
       uint32_t word = 0u;
-      if (base != nullptr) {
-        const uint32_t src0 = al[e >> 2], src1 = al[(e + 1) >> 2];
-        const float v0 = __uint_as_float(__byte_perm(src0, 0x4B000000u, 0x7540u + (e & 3))) - 8388608.0f;
-        const float v1 = __uint_as_float(__byte_perm(src1, 0x4B000000u, 0x7540u + ((e + 1) & 3))) - 8388608.0f;
-        const float x0 = fmaf(v0, sc[e % 3], sh[e % 3]);
-        const float x1 = fmaf(v1, sc[(e + 1) % 3], sh[(e + 1) % 3]);
-        __nv_bfloat162 p2 = __floats2bfloat162_rn(x0, x1);
+      if (ph < P && base != nullptr) {
+        const uint32_t b0 = __byte_perm(al[e >> 2], 0x4B000000u, 0x7540u + (e & 3));
+        const uint32_t b1 = __byte_perm(al[(e + 1) >> 2], 0x4B000000u, 0x7540u + ((e + 1) & 3));
+        uint32_t x0, x1;
+        unpack2(norm2(pack2(b0, b1), sc2[e % 3], sh2[e % 3]), x0, x1);
+        __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(x0), __uint_as_float(x1));
         word = *reinterpret_cast<uint32_t*>(&p2);
       }
-      const int kw = (ph * RUN + e) >> 1;
-      if (!emit_word(kw, word)) return false;
+      const int kw = (row_start + e) >> 1;     // bf16 pair inside the slice
+      cw[kw & 3] = word;
+      if ((kw & 3) == 3) {
+        const int kc = kw >> 2;                // chunk of 8 features
+        const int j = kc >> 3;                 // K block
+        const int q = kc & 7;                  // chunk inside the 128-byte row
+        const uint32_t addr = a_smem + (uint32_t)j * kABlockBytes + row_off + (((uint32_t)q ^ swz) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(cw[0]), "r"(cw[1]), "r"(cw[2]),
+                     "r"(cw[3])
+                     : "memory");
+        if (q == 7 || kc == KEND / 8 - 1) {
+          // this thread's generic-proxy writes to its own CTA's shared memory become
+          // visible to the tensor core; one release arrive per warp on the even CTA
+          fence_proxy_async_smem();
+          __syncwarp();
+          if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(a_full_leader + 8u * (uint32_t)j);
+          if (j + 1 < JE) {
+            VITFE_ROWS_OF_BLOCK(j + 1);
+            if (!mbar_wait_cl(a_empty0 + 8u * (uint32_t)(j + 1), empty_parity, abort_flag, limit_ns, 128))
+              return false;
+          }
+        }
+      }
     }
   }
-  // zero features [KS, KEND) of the last K16 step
-#pragma unroll
-  for (int k = KS; k < KEND; k += 2)
-    if (!emit_word(k >> 1, 0u)) return false;
-  (void)NBLK;
+#undef VITFE_ROWS_OF_BLOCK
+#undef VITFE_LOAD_ROW
   return true;
 }
 
@@ -275,7 +341,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     hs->abort_flag = 0;
     for (int j = 0; j < NBLK; ++j) {
-      mbar_init(smem_u32(&hs->a_full[j]), 2 * kProducerThreads);
+      mbar_init(smem_u32(&hs->a_full[j]), 2 * (kProducerThreads / 32));   // one arrive per producer warp
       mbar_init(smem_u32(&hs->a_empty[j]), 1);
     }
     for (int s = 0; s < args.nstage; ++s) {
@@ -310,17 +376,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t acc_empty_L = mapa_shared(smem_u32(&hs->acc_empty[0]), 0);
 
   // ---- roles -------------------------------------------------------------
-  if (warp < 4) {
-    // A producers: this CTA's 128 rows of every pair tile
+  if (warp < kProducerWarps) {
+    // A producers: this CTA's 128 rows of every pair tile, K blocks split in two halves
     const float sc[3] = {args.scale0, args.scale1, args.scale2};
     const float sh[3] = {args.shift0, args.shift1, args.shift2};
-    const int row = threadIdx.x;
+    const int row = threadIdx.x & (kProducerThreads - 1);
+    const int half = threadIdx.x / kProducerThreads;
     const int rofs = (int)rank * kTileM + row;
     uint32_t np = 0;
     bool ok = true;
     int tile = cid;
     RowSrc cur = tile < args.num_tiles ? row_src<P>(args, hs, tile * kPairRows + rofs) : RowSrc{nullptr, 0, 0};
-    prefetch_row<P>(cur, args.T);
+    if (half == 0) prefetch_row<P>(cur, args.T);
     for (; ok && tile < args.num_tiles; tile += ncl) {
       const int kind = tile_kind(tile * kPairRows, hs, args.T);
       const int next = tile + ncl;
@@ -330,40 +397,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int q = 0; ok && q < nprod; ++q) {
           const int s = (kind == kResident) ? 0 : (q % args.T);
           const uint8_t* base = cur.base0 ? cur.base0 + cur.fstride * s : nullptr;
-          ok = produce_slice<P>(base, cur.rs, a_smem, hs, np, row, sc, sh, abort_flag, args.limit_ns, a_full_L);
+          if (half == 0)
+            ok = produce_blocks<P, 0, NBLK / 2>(base, cur.rs, a_smem, hs, np, row, sc, sh, abort_flag,
+                                                args.limit_ns, a_full_L);
+          else
+            ok = produce_blocks<P, NBLK / 2, NBLK>(base, cur.rs, a_smem, hs, np, row, sc, sh, abort_flag,
+                                                   args.limit_ns, a_full_L);
           ++np;
-          if (q == 0) prefetch_row<P>(nxt, args.T);
+          if (q == 0 && half == 0) prefetch_row<P>(nxt, args.T);
         }
       }
       cur = nxt;
     }
   } else if (warp == kTmaWarp) {
     if (lane == 0) {
+      // W tiles in consumption order: one stage per step (a step = one 64-feature K block
+      // of one temporal slice)
       uint32_t nb = 0, stage = 0, bphase = 0;
       bool ok = true;
       for (int tile = cid; ok && tile < args.num_tiles; tile += ncl) {
         const int kind = tile_kind(tile * kPairRows, hs, args.T);
         if (kind == kPad) continue;
+        const int nsteps = args.T * NBLK;
         for (int p = 0; ok && p < args.npass; ++p) {
           const int n0 = p * args.bn;
           const int npw = min(args.bn, args.N - n0);
           const int c1 = n0 + (int)rank * (npw / 2);
-          const int nouter = (kind == kResident) ? NBLK : args.T;
-          const int ninner = (kind == kResident) ? args.T : NBLK;
-          for (int o = 0; ok && o < nouter; ++o) {
-            for (int in = 0; ok && in < ninner; ++in) {
-              const int j = (kind == kResident) ? o : in;
-              const int s = (kind == kResident) ? in : o;
-              if (!mbar_wait_cl(smem_u32(&hs->b_empty[stage]), bphase ^ 1u, abort_flag, args.limit_ns)) {
-                ok = false;
-                break;
-              }
-              if (leader) mbar_arrive_expect_tx(smem_u32(&hs->b_full[stage]), 2u * b_stage_bytes);
-              tma_load_2d_pair(b_smem + stage * b_stage_bytes, &tmap_w, b_full_L + 8u * stage,
-                               s * args.kslice_pad + 64 * j, c1);
-              ++nb;
-              if (++stage == (uint32_t)args.nstage) { stage = 0; bphase ^= 1u; }
+          for (int st = 0; ok && st < nsteps; ++st) {
+            const int j = (kind == kResident) ? st / args.T : st % NBLK;
+            const int sl = (kind == kResident) ? st % args.T : st / NBLK;
+            if (!mbar_wait_cl(smem_u32(&hs->b_empty[stage]), bphase ^ 1u, abort_flag, args.limit_ns)) {
+              ok = false;
+              break;
             }
+            if (leader) mbar_arrive_expect_tx(smem_u32(&hs->b_full[stage]), 2u * b_stage_bytes);
+            tma_load_2d_pair(b_smem + stage * b_stage_bytes, &tmap_w, b_full_L + 8u * stage,
+                             sl * args.kslice_pad + 64 * j, c1);
+            ++nb;
+            if (++stage == (uint32_t)args.nstage) { stage = 0; bphase ^= 1u; }
           }
         }
       }
@@ -388,28 +459,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0 && leader) {
-      // The tensor core queues few MMAs: everything this thread does between MMA
-      // issues is kept to a minimum (precomputed descriptors, CTA-scope waits on the
-      // TMA barriers, unrolled K blocks).
+      // The single issuing thread is the throughput limiter (each tcgen05.mma issue costs
+      // it tens of cycles), so the code between issues is minimal: descriptors at
+      // constant offsets, a one-instruction fast path for barriers already complete.
       uint32_t na = 0, np = 0, stage = 0, bphase = 0;
       bool ok = true;
       const uint64_t adesc0 = sw128_desc(a_smem);
       const uint64_t bdesc0 = sw128_desc(b_smem);
-      const uint64_t bstage_desc = (uint64_t)(b_stage_bytes >> 4);
-      auto b_step = [&](uint64_t adesc, int nk, uint32_t d_tmem, uint32_t idesc, uint32_t& accum) -> bool {
-        if (!mbar_wait(smem_u32(&hs->b_full[stage]), bphase, abort_flag, args.limit_ns)) return false;
-        const uint64_t bdesc = bdesc0 + bstage_desc * stage;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          if (kk < nk) {
-            umma_bf16_pair(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc, accum);
-            accum = 1;
-          }
-        }
-        umma_commit_pair(smem_u32(&hs->b_empty[stage]));
-        if (++stage == (uint32_t)args.nstage) { stage = 0; bphase ^= 1u; }
-        return true;
-      };
+      const uint64_t bstep = (uint64_t)(b_stage_bytes >> 4);
+      uint64_t bd_cur = bdesc0;
+      const uint32_t b_full0 = smem_u32(&hs->b_full[0]);
+      const uint32_t b_empty0 = smem_u32(&hs->b_empty[0]);
+      const uint32_t a_full0 = smem_u32(&hs->a_full[0]);
+      const uint32_t a_empty0 = smem_u32(&hs->a_empty[0]);
+      const uint32_t nstage = (uint32_t)args.nstage;
+      const int T = args.T;
+
+#define VITFE_WAIT_B()                                                                        \
+  do {                                                                                        \
+    const uint32_t bar_ = b_full0 + 8u * stage;                                               \
+    if (!mbar_try_wait(bar_, bphase) && !mbar_wait(bar_, bphase, abort_flag, args.limit_ns))  \
+      ok = false;                                                                             \
+  } while (0)
+#define VITFE_WAIT_A(J)                                                                       \
+  do {                                                                                        \
+    const uint32_t abar_ = a_full0 + 8u * (J);                                                \
+    if (!mbar_try_wait_cluster(abar_, np & 1u) && !mbar_wait_cl(abar_, np & 1u, abort_flag, args.limit_ns)) \
+      ok = false;                                                                             \
+  } while (0)
+#define VITFE_STEP(ADESC, NK, FIRST)                                                          \
+  do {                                                                                        \
+    const uint64_t bd_ = bd_cur;                                                              \
+    umma_bf16_pair(d_tmem, (ADESC), bd_, idesc, (FIRST) ? 0u : 1u);                           \
+    if ((NK) > 1) umma_bf16_pair(d_tmem, (ADESC) + 2u, bd_ + 2u, idesc, 1u);                 \
+    if ((NK) > 2) umma_bf16_pair(d_tmem, (ADESC) + 4u, bd_ + 4u, idesc, 1u);                 \
+    if ((NK) > 3) umma_bf16_pair(d_tmem, (ADESC) + 6u, bd_ + 6u, idesc, 1u);                 \
+    umma_commit_pair(b_empty0 + 8u * stage);                                                  \
+    if (++stage == nstage) {                                                                  \
+      stage = 0;                                                                              \
+      bphase ^= 1u;                                                                           \
+      bd_cur = bdesc0;                                                                        \
+    } else {                                                                                  \
+      bd_cur += bstep;                                                                        \
+    }                                                                                         \
+  } while (0)
+
       for (int tile = cid; ok && tile < args.num_tiles; tile += ncl) {
         const int kind = tile_kind(tile * kPairRows, hs, args.T);
         if (kind == kPad) continue;
@@ -423,32 +517,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int npw = min(args.bn, args.N - p * args.bn);
           const uint32_t idesc = idesc_bf16(kPairRows, npw);
           const uint32_t d_tmem = tmem + buf * (uint32_t)args.bn;
-          uint32_t accum = 0;
           if (kind == kResident) {
             // one resident slice of A feeds every temporal slice of W
 #pragma unroll
             for (int j = 0; j < NBLK; ++j) {
-              if (p == 0) {
-                if (!mbar_wait_cl(smem_u32(&hs->a_full[j]), np & 1u, abort_flag, args.limit_ns)) { ok = false; break; }
-                tc_fence_after();
+              if (p == 0) VITFE_WAIT_A(j);
+              const uint64_t ad = adesc0 + (uint64_t)(j * (kABlockBytes >> 4));
+              for (int sl = 0; ok && sl < T; ++sl) {
+                VITFE_WAIT_B();
+                if (!ok) break;
+                VITFE_STEP(ad, ksteps_of<P>(j), j == 0 && sl == 0);
               }
-              const uint64_t adesc = adesc0 + (uint64_t)(j * (kABlockBytes >> 4));
-              for (int s = 0; s < args.T; ++s)
-                if (!b_step(adesc, ksteps_of<P>(j), d_tmem, idesc, accum)) { ok = false; break; }
               if (!ok) break;
-              if (p == args.npass - 1) umma_commit_pair(smem_u32(&hs->a_empty[j]));
+              if (p == args.npass - 1) umma_commit_pair(a_empty0 + 8u * j);
             }
           } else {
-            for (int s = 0; ok && s < args.T; ++s) {
+            for (int sl = 0; ok && sl < T; ++sl) {
 #pragma unroll
               for (int j = 0; j < NBLK; ++j) {
-                if (!mbar_wait_cl(smem_u32(&hs->a_full[j]), np & 1u, abort_flag, args.limit_ns)) { ok = false; break; }
-                tc_fence_after();
-                if (!b_step(adesc0 + (uint64_t)(j * (kABlockBytes >> 4)), ksteps_of<P>(j), d_tmem, idesc, accum)) {
-                  ok = false;
-                  break;
-                }
-                umma_commit_pair(smem_u32(&hs->a_empty[j]));
+                VITFE_WAIT_A(j);
+                VITFE_WAIT_B();
+                if (!ok) break;
+                VITFE_STEP(adesc0 + (uint64_t)(j * (kABlockBytes >> 4)), ksteps_of<P>(j), sl == 0 && j == 0);
+                umma_commit_pair(a_empty0 + 8u * j);
               }
               ++np;   // one slice production consumed
             }
@@ -459,6 +550,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (kind == kResident) ++np;
       }
+#undef VITFE_STEP
+#undef VITFE_WAIT_A
+#undef VITFE_WAIT_B
       if (!ok) {
         umma_commit_pair(smem_u32(&hs->drain));
         const uint64_t t0 = global_timer_ns();
@@ -466,11 +560,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
-    // epilogue warps 4..11: lane quarter q = warp % 4 of this CTA's accumulator rows,
-    // column half h of every pass
+  } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
+    // epilogue: lane quarter q = warp % 4 of this CTA's accumulator rows
     const int q = warp & 3;
-    const int h = (warp - 4) >> 2;
     const int rloc = (int)rank * kTileM + q * 32 + lane;
     const bool out32 = (reinterpret_cast<uintptr_t>(args.out) & 31u) == 0;
     uint32_t na = 0;
@@ -489,8 +581,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (kind == kPad) {
         if (in_bucket) {
           const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-          const int half = args.N / 2;
-          for (int c = h * half; c < (h + 1) * half; c += 8) *reinterpret_cast<uint4*>(orow + c) = z;
+          for (int c = 0; c < args.N; c += 8) *reinterpret_cast<uint4*>(orow + c) = z;
         }
         continue;
       }
@@ -502,19 +593,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const int npw = min(args.bn, args.N - p * args.bn);
-        const int cw = npw / 2;     // columns of this warp (a multiple of 16)
-        for (int c0 = h * cw; c0 < (h + 1) * cw; c0 += 32) {
+        for (int c0 = 0; c0 < npw; c0 += 32) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + buf * (uint32_t)args.bn + (uint32_t)c0, v);
           tmem_wait_ld();
-          const int ncol = min(32, (h + 1) * cw - c0);   // 32, or 16 for a 16-column tail
           if (in_bucket) {
             const int n0 = p * args.bn + c0;
             uint32_t pk[16];
             const float4* bias4 = reinterpret_cast<const float4*>(args.bias + n0);
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
-              const float4 bv = e4 * 4 < ncol ? __ldg(bias4 + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+              const float4 bv = __ldg(bias4 + e4);
               __nv_bfloat162 b0 = __floats2bfloat162_rn(__uint_as_float(v[4 * e4]) + bv.x,
                                                         __uint_as_float(v[4 * e4 + 1]) + bv.y);
               __nv_bfloat162 b1 = __floats2bfloat162_rn(__uint_as_float(v[4 * e4 + 2]) + bv.z,
@@ -525,15 +614,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __nv_bfloat16* dst = orow + n0;
             if (out32) {
               st_global_v8(dst, pk);
-              if (ncol == 32) st_global_v8(dst + 16, pk + 8);
+              st_global_v8(dst + 16, pk + 8);
             } else {
               uint4* d4 = reinterpret_cast<uint4*>(dst);
-              __stcs(d4, make_uint4(pk[0], pk[1], pk[2], pk[3]));
-              __stcs(d4 + 1, make_uint4(pk[4], pk[5], pk[6], pk[7]));
-              if (ncol == 32) {
-                __stcs(d4 + 2, make_uint4(pk[8], pk[9], pk[10], pk[11]));
-                __stcs(d4 + 3, make_uint4(pk[12], pk[13], pk[14], pk[15]));
-              }
+#pragma unroll
+              for (int e = 0; e < 4; ++e) __stcs(d4 + e, make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]));
             }
           }
         }
@@ -570,16 +655,21 @@ cudaError_t embed_configure(Ctx& c) {
   int max_optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
   if (e != cudaSuccess) return e;
-  const int bn = c.N < 256 ? c.N : 256;
-  for (int nst = 8; nst >= 2; --nst) {
-    const size_t need = embed_smem_bytes(c.nblk, bn / 2, nst);
-    if (need <= (size_t)max_optin) {
-      c.bn = bn;
-      c.nstage = nst;
-      c.embed_smem = need;
-      c.embed_ok = true;
-      break;
+  // widest N tile first (fewest MMA issues per flop); a stage holds this CTA's half of
+  // one W tile, and at least two stages must fit beside the resident A slice
+  for (int bn : {256, 128}) {
+    if (bn > c.N && bn != 128) continue;
+    const int b = bn < c.N ? bn : c.N;
+    for (int nst = 8; nst >= 2 && !c.embed_ok; --nst) {
+      const size_t need = embed_smem_bytes(c.nblk, b / 2, nst);
+      if (need <= (size_t)max_optin) {
+        c.bn = b;
+        c.nstage = nst;
+        c.embed_smem = need;
+        c.embed_ok = true;
+      }
     }
+    if (c.embed_ok) break;
   }
   if (!c.embed_ok) return cudaSuccess;
   const void* fn = (c.P == 14) ? (const void*)embed_kernel<14> : (const void*)embed_kernel<16>;
