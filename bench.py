@@ -343,6 +343,24 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
 
+    # standalone normalise + patchify (HBM-bound side path), timed alone
+    flat = torch.empty((rows, K), dtype=torch.bfloat16, device=dev)
+    np_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(8):
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            B.vitfe_normalize_patchify(fe.h, batch.pixels, batch.pixel_bytes, batch.items, batch.n_items,
+                                       batch.capacity, rows, flat, None, stream)
+            a1.record(stream)
+            a1.synchronize()
+            if i >= 3:
+                np_ms.append(a0.elapsed_time(a1))
+    np_ms = statistics.median(np_ms)
+    np_bytes = batch.pixel_bytes + rows * K * 2
+    del flat
+
     pk, pk_kind = peaks()
     flops = 2.0 * rows * K * N
     achieved = flops / (embed_ms / 1e3) / 1e12
@@ -363,7 +381,11 @@ def main():
                      "kernel": "embed_kernel<14>", "flops_per_launch": flops,
                      "kernel_ms": embed_ms},
         "side_paths": {"rope_ms": rope_ms,
-                       "rope_gbs": rows * wl.head_dim // 2 * 4 * 2 / (rope_ms / 1e3) / 1e9},
+                       "rope_gbs": rows * wl.head_dim // 2 * 4 * 2 / (rope_ms / 1e3) / 1e9,
+                       "rope_frac_hbm": rows * wl.head_dim // 2 * 4 * 2 / (rope_ms / 1e3) / 1e9 / float(pk["hbm_gbs"]),
+                       "normalize_patchify_ms": np_ms,
+                       "normalize_patchify_gbs": np_bytes / (np_ms / 1e3) / 1e9,
+                       "normalize_patchify_frac_hbm": np_bytes / (np_ms / 1e3) / 1e9 / float(pk["hbm_gbs"])},
         "e2e": {"value": world * rows / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": 3 * args.steps,

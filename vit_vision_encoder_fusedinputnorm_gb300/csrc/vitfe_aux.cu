@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(kAuxThreads) pos_ids_kernel(const vitfe_item* 
 // ---------------------------------------------------------------------------
 // 2D-RoPE ("vLLM 多模态推理｜ViT 性能优化" §3.3 steps 1, 3, 5)
 // ---------------------------------------------------------------------------
+__device__ void rope_fill(float* tab, int nf, double theta, int maxside);
+
 // Axis table: tab[0][p][i] = cos(p * w_i), tab[1][p][i] = sin(p * w_i), w_i = theta^(-2i/d),
 // d = head_dim / 2, i < nf = head_dim / 4, p < max(h, w) over the call's items.
 // Angles and cos/sin in fp64, rounded once to fp32.
@@ -62,6 +64,15 @@ __global__ void __launch_bounds__(kAuxThreads) rope_table_kernel(const vitfe_ite
     build_item_table(items, n_items, max_items, -1, 1, T, M, rows, VITFE_ROPE_MAX_SIDE, st.tab());
   __syncthreads();
   const int maxside = st.hdr.maxside;
+  rope_fill(tab, nf, theta, maxside);
+}
+
+// Every position of the table: the handle's cos/sin cache, built once per (head_dim, theta).
+__global__ void __launch_bounds__(kAuxThreads) rope_cache_kernel(int nf, double theta, float* tab) {
+  rope_fill(tab, nf, theta, VITFE_ROPE_MAX_SIDE);
+}
+
+__device__ void rope_fill(float* tab, int nf, double theta, int maxside) {
   const double d = 2.0 * nf;
   const int total = maxside * nf;
   for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x) {
@@ -93,6 +104,7 @@ __global__ void __launch_bounds__(kAuxThreads) rope_expand_kernel(const vitfe_it
   const int nvec = width >> 2;       // float4 per row
   const float* tc = tab;
   const float* ts = tab + (size_t)VITFE_ROPE_MAX_SIDE * nf;
+  const bool vec_tab = (nf % 4) == 0;   // table rows 16-byte aligned, halves whole float4 groups
   for (int wbase = (blockIdx.x * wpb + (threadIdx.x >> 5)) * 32; wbase < rows; wbase += gridDim.x * wpb * 32) {
     const int2 mypos = row_pos(wbase + lane, st, items, M);
     const int cnt = min(32, rows - wbase);
@@ -107,22 +119,32 @@ __global__ void __launch_bounds__(kAuxThreads) rope_expand_kernel(const vitfe_it
       const int wp = __shfl_sync(0xffffffffu, mypos.y, rr);
       if (f < total) {
         const int cv = f - rr * nvec;
-        float cvals[4], svals[4];
+        float4 cvv, svv;
+        if (hp < 0) {
+          cvv = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+          svv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        } else if (vec_tab) {
+          // each group of 4 columns lies in one half: one 16-byte load per table
+          const int col = 4 * cv;
+          const int p = col < nf ? hp : wp;
+          const int i = col < nf ? col : col - nf;
+          cvv = __ldg(reinterpret_cast<const float4*>(tc + (size_t)p * nf + i));
+          svv = __ldg(reinterpret_cast<const float4*>(ts + (size_t)p * nf + i));
+        } else {
+          float cvals[4], svals[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int col = 4 * cv + e;
-          if (hp < 0) {
-            cvals[e] = 1.0f;
-            svals[e] = 0.0f;
-          } else {
+          for (int e = 0; e < 4; ++e) {
+            const int col = 4 * cv + e;
             const int p = col < nf ? hp : wp;
             const int i = col < nf ? col : col - nf;
             cvals[e] = __ldg(tc + (size_t)p * nf + i);
             svals[e] = __ldg(ts + (size_t)p * nf + i);
           }
+          cvv = make_float4(cvals[0], cvals[1], cvals[2], cvals[3]);
+          svv = make_float4(svals[0], svals[1], svals[2], svals[3]);
         }
-        __stcs(cdst + f, make_float4(cvals[0], cvals[1], cvals[2], cvals[3]));
-        __stcs(sdst + f, make_float4(svals[0], svals[1], svals[2], svals[3]));
+        __stcs(cdst + f, cvv);
+        __stcs(sdst + f, svv);
       }
     }
   }
@@ -288,6 +310,210 @@ __global__ void __launch_bounds__(kAuxThreads) normalize_patchify_kernel(const N
   }
 }
 
+// Specialised for patch P (14, 16) and tpatch T (1, 2).  Each warp owns two output rows at
+// a time, end to end: lanes 0-1 decode the rows, one lane per (row, pixel row ph) loads the
+// 3P-byte run of each stored frame once (aligned 4-byte loads) and writes, for every channel
+// c and temporal slice t, the P features (c, t, ph, 0..P-1) of the canonical order into the
+// warp's shared-memory copy of the two rows, which the warp then writes out with contiguous
+// 16-byte stores (the rows are adjacent in the output).  The loads of the warp's next pair
+// are issued before the current pair is converted, so every warp keeps one pair of pixel
+// runs in flight while it converts and writes; there is no CTA-wide barrier in the loop.
+constexpr int kNpWarpRows = 2;
+
+// Two fp32 lanes in one 64-bit register (packed f32x2 arithmetic, exact per lane).
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, uint32_t& lo, uint32_t& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+// x = (v - 2^23) * scale + shift on both lanes; v holds 2^23 + byte (exact).
+__device__ __forceinline__ uint64_t norm2(uint64_t v, uint64_t scale2, uint64_t shift2) {
+  const uint64_t m = 0xCB000000CB000000ull;   // (-2^23, -2^23)
+  uint64_t t, x;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(t) : "l"(v), "l"(m));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(x) : "l"(t), "l"(scale2), "l"(shift2));
+  return x;
+}
+
+// Stage row stride (32-bit words): the features (c, t, ph, pw..pw+1) of lane (row, ph) sit
+// at row * RS + ((c * T + t) * P + ph) * P / 2 + pw / 2, so one store instruction touches
+// banks (P/2) * ph + RS * row (mod 32).  For P = 14 the 14 banks of one row are distinct and
+// RS = 16 (mod 32) keeps the second row's 14 off them; for P = 16 a row covers 4 banks and
+// RS = 4 (mod 32) at least keeps the rows apart.  RS stays a multiple of 4 (16-byte reads).
+__host__ __device__ constexpr int np_stage_rs(int P, int KW) {
+  return KW + ((((P == 14) ? 16 : 4) - KW % 32) + 32) % 32;
+}
+
+template <int P, int T>
+struct NpPair {
+  static constexpr int RUN = 3 * P;                 // bytes of one pixel row of one patch
+  static constexpr int NW = (RUN + 3) / 4 + 1;      // aligned words covering it
+  uint32_t raw[T][NW];
+  uint32_t sft;                                     // byte offset of the run in raw[.][0]
+  int flag;                                         // bit 0: row valid, bit 1: still item
+  int nrows;                                        // rows of this pair inside [0, rows)
+};
+
+// Decode rows rb, rb + 1 and issue this lane's loads (lane = row * P + ph).
+template <int P, int T>
+__device__ __forceinline__ void np_fetch(NpPair<P, T>& q, const NpArgs& a, const SmemTab& st, int rb,
+                                         int lane) {
+  q.nrows = min(kNpWarpRows, a.rows - rb);
+  int flag = 0;
+  unsigned long long b0 = 0ull;
+  long long rs = 0, fs = 0;
+  if (lane < q.nrows) {
+    const int r = rb + lane;
+    if (r < st.hdr.live) {
+      const int i = find_item(st.start, st.hdr.n, r);
+      if (!tab_bit(st.bad, i)) {
+        const vitfe_item it = a.items[i];
+        int tg, hh, ww;
+        decode_local(r - st.start[i], it.h, it.w, a.M, tg, hh, ww);
+        const int64_t H = (int64_t)it.h * P, W = (int64_t)it.w * P;
+        const bool still = it.frames == 1;
+        rs = W * 3;
+        fs = still ? 0 : H * W * 3;
+        const int64_t f0 = still ? 0 : (int64_t)tg * T;
+        b0 = reinterpret_cast<unsigned long long>(a.pixels + it.pixel_offset +
+                                                  ((f0 * H + (int64_t)hh * P) * W + (int64_t)ww * P) * 3);
+        flag = 1 | (still ? 2 : 0);
+      }
+    }
+  }
+  const int lr = lane / P;
+  const int ph = lane - lr * P;
+  q.flag = __shfl_sync(0xffffffffu, flag, lr);
+  const unsigned long long base = __shfl_sync(0xffffffffu, b0, lr);
+  const long long mrs = __shfl_sync(0xffffffffu, rs, lr);
+  const long long mfs = __shfl_sync(0xffffffffu, fs, lr);
+  if (lr >= q.nrows) q.flag = 0;
+  const uintptr_t addr0 = (uintptr_t)(base + (unsigned long long)(mrs * ph));
+  q.sft = (uint32_t)(addr0 & 3u);
+#pragma unroll
+  for (int tt = 0; tt < T; ++tt) {
+    // a still's one frame serves every temporal slice: load it once
+    const bool ld = (q.flag & 1) && (tt == 0 || !(q.flag & 2));
+    const uint32_t* w0 = reinterpret_cast<const uint32_t*>((addr0 + (uintptr_t)(mfs * tt)) & ~uintptr_t(3));
+#pragma unroll
+    for (int w = 0; w < NpPair<P, T>::NW; ++w)
+      q.raw[tt][w] = (ld && 4u * w < q.sft + NpPair<P, T>::RUN) ? __ldg(w0 + w) : 0u;
+  }
+}
+
+// Convert this lane's runs into the stage (row lr, pixel row ph).
+template <int P, int T>
+__device__ __forceinline__ void np_convert(const NpPair<P, T>& q, uint32_t* srow, int ph, const float* sc,
+                                           const float* sh) {
+  constexpr int NA = (3 * P + 3) / 4;
+  const bool valid = q.flag & 1;
+  const bool still = q.flag & 2;
+  const uint32_t sel = 0x3210u + 0x1111u * q.sft;
+#pragma unroll
+  for (int tt = 0; tt < T; ++tt) {
+    if (tt > 0 && still) break;
+    uint32_t al[NA];
+#pragma unroll
+    for (int w = 0; w < NA; ++w) al[w] = __byte_perm(q.raw[tt][w], q.raw[tt][w + 1], sel);
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+      const uint64_t s2 = pack2(__float_as_uint(sc[c]), __float_as_uint(sc[c]));
+      const uint64_t h2 = pack2(__float_as_uint(sh[c]), __float_as_uint(sh[c]));
+#pragma unroll
+      for (int pw = 0; pw < P; pw += 2) {
+        const int e0 = 3 * pw + c, e1 = 3 * (pw + 1) + c;
+        const uint32_t v0 = __byte_perm(al[e0 >> 2], 0x4B000000u, 0x7540u + (e0 & 3));
+        const uint32_t v1 = __byte_perm(al[e1 >> 2], 0x4B000000u, 0x7540u + (e1 & 3));
+        uint32_t x0, x1;
+        unpack2(norm2(pack2(v0, v1), s2, h2), x0, x1);
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(x0), __uint_as_float(x1));
+        const uint32_t word = valid ? *reinterpret_cast<uint32_t*>(&b2) : 0u;
+        if (still) {
+#pragma unroll
+          for (int t2 = 0; t2 < T; ++t2) srow[(((c * T + t2) * P + ph) * P + pw) >> 1] = word;
+        } else {
+          srow[(((c * T + tt) * P + ph) * P + pw) >> 1] = word;
+        }
+      }
+    }
+  }
+}
+
+template <int P, int T>
+__global__ void __launch_bounds__(kAuxThreads) normalize_patchify_p_kernel(const NpArgs a) {
+  constexpr int KW = 3 * T * P * P / 2;                     // bf16 pairs per row
+  constexpr int RS = np_stage_rs(P, KW);
+  static_assert(KW % 4 == 0 && RS % 4 == 0, "16-byte rows");
+  static_assert(kNpWarpRows * P <= 32, "one lane per (row, pixel row)");
+  extern __shared__ __align__(16) uint8_t np_smem[];
+  __shared__ SmemTab st;
+  if (threadIdx.x < 32)
+    build_item_table(a.items, a.n_items, a.max_items, a.pixel_bytes, P, a.T, a.M, a.rows, 0x7fffffff, st.tab());
+  __syncthreads();
+  write_status(a.status, &st.hdr);
+  const float sc[3] = {a.sc0, a.sc1, a.sc2};
+  const float sh[3] = {a.sh0, a.sh1, a.sh2};
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int wpb = blockDim.x >> 5;
+  uint32_t* stage = reinterpret_cast<uint32_t*>(np_smem) + (size_t)warp * (RS + KW);
+  const int lr = lane / P;
+  const int ph = lane - lr * P;
+  const int step = gridDim.x * wpb * kNpWarpRows;
+  int rb = (blockIdx.x * wpb + warp) * kNpWarpRows;
+  if (rb >= a.rows) return;
+  NpPair<P, T> cur;
+  np_fetch<P, T>(cur, a, st, rb, lane);
+  for (;;) {
+    const int rn = rb + step;
+    NpPair<P, T> nxt;
+    if (rn < a.rows) np_fetch<P, T>(nxt, a, st, rn, lane);
+    if (lr < cur.nrows) np_convert<P, T>(cur, stage + lr * RS, ph, sc, sh);
+    __syncwarp();
+    // the two rows are adjacent in the output: write them with 16-byte stores
+    constexpr int KW4 = KW / 4, GAP4 = (RS - KW) / 4;
+    const int nvec = cur.nrows * KW4;
+    uint4* dst = reinterpret_cast<uint4*>(a.out) + (size_t)rb * KW4;
+    const uint4* src = reinterpret_cast<const uint4*>(stage);
+    for (int v = lane; v < nvec; v += 32) __stcs(dst + v, src[v + (v >= KW4 ? GAP4 : 0)]);
+    __syncwarp();
+    if (rn >= a.rows) break;
+    cur = nxt;
+    rb = rn;
+  }
+}
+
+int grid_for(long long work, int per_cta, int cap) {
+  long long g = (work + per_cta - 1) / per_cta;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return (int)g;
+}
+
+template <int P, int T>
+cudaError_t launch_np_p(const Ctx& c, const NpArgs& a, cudaStream_t s) {
+  constexpr int KW = 3 * T * P * P / 2;
+  constexpr int RS = np_stage_rs(P, KW);
+  const size_t stage_bytes = (size_t)(kAuxThreads / 32) * (RS + KW) * 4;
+  static int per_sm = 0;     // resident CTAs per SM (same on every device of one kind), queried once
+  if (per_sm == 0) {
+    cudaError_t e = cudaFuncSetAttribute(normalize_patchify_p_kernel<P, T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stage_bytes);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, normalize_patchify_p_kernel<P, T>, kAuxThreads,
+                                                      stage_bytes);
+    if (e != cudaSuccess) return e;
+    per_sm = n > 0 ? n : 1;
+  }
+  const int grid = grid_for(a.rows, (kAuxThreads / 32) * kNpWarpRows, c.sm_count * per_sm);
+  normalize_patchify_p_kernel<P, T><<<grid, kAuxThreads, stage_bytes, s>>>(a);
+  return cudaGetLastError();
+}
+
 size_t np_smem_bytes(int P, int T, int K, int nwr) {
   size_t off = (sizeof(SmemTab) + 15) & ~size_t(15);
   off += ((size_t)K * 4 + 15) & ~size_t(15);
@@ -328,12 +554,6 @@ __global__ void permute_weight_kernel(const __nv_bfloat16* __restrict__ W, const
   }
 }
 
-int grid_for(long long work, int per_cta, int cap) {
-  long long g = (work + per_cta - 1) / per_cta;
-  if (g < 1) g = 1;
-  if (g > cap) g = cap;
-  return (int)g;
-}
 
 }  // namespace
 
@@ -345,17 +565,31 @@ cudaError_t launch_pos_ids(const Ctx& c, const vitfe_item* items, const int32_t*
   return cudaGetLastError();
 }
 
-cudaError_t launch_rope(const Ctx& c, const vitfe_item* items, const int32_t* n_items, int max_items,
-                        int64_t rows, int head_dim, float theta, float* cos, float* sin, int32_t* status,
-                        cudaStream_t s) {
+cudaError_t launch_rope(Ctx& c, const vitfe_item* items, const int32_t* n_items, int max_items, int64_t rows,
+                        int head_dim, float theta, float* cos, float* sin, int32_t* status, cudaStream_t s) {
   const int nf = head_dim / 4;
-  rope_table_kernel<<<32, kAuxThreads, 0, s>>>(items, n_items, max_items, c.T, c.M, (int)rows, nf,
-                                               (double)theta, c.rope_tab);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  const size_t slot_floats = (size_t)2 * VITFE_ROPE_MAX_SIDE * (VITFE_ROPE_MAX_HEAD_DIM / 4);
+  // the cos/sin cache of this (head_dim, theta): built once over every position, then reused
+  int slot = -1;
+  for (int k = 0; k < Ctx::kRopeSlots; ++k)
+    if (c.rope_hd[k] == head_dim && c.rope_theta[k] == theta) slot = k;
+  float* tab;
+  if (slot < 0) {
+    slot = c.rope_next;
+    c.rope_next = (c.rope_next + 1) % Ctx::kRopeSlots;
+    tab = c.rope_tab + (size_t)slot * slot_floats;
+    rope_cache_kernel<<<grid_for((long long)VITFE_ROPE_MAX_SIDE * nf, kAuxThreads, c.sm_count * 4), kAuxThreads, 0,
+                        s>>>(nf, (double)theta, tab);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    c.rope_hd[slot] = head_dim;
+    c.rope_theta[slot] = theta;
+  } else {
+    tab = c.rope_tab + (size_t)slot * slot_floats;
+  }
   const int grid = grid_for(rows, kAuxThreads, c.sm_count * 16);   // 8 warps x 32 rows per CTA
-  rope_expand_kernel<<<grid, kAuxThreads, 0, s>>>(items, n_items, max_items, c.T, c.M, (int)rows, nf,
-                                                  c.rope_tab, cos, sin, status);
+  rope_expand_kernel<<<grid, kAuxThreads, 0, s>>>(items, n_items, max_items, c.T, c.M, (int)rows, nf, tab, cos, sin,
+                                                  status);
   return cudaGetLastError();
 }
 
@@ -378,6 +612,9 @@ cudaError_t launch_normalize_patchify(const Ctx& c, const uint8_t* pixels, int64
   a.M = c.M;
   a.K = c.K;
   a.nwr = (3 * c.P + 3) / 4 + 1;
+  if (c.P == 14 && c.T == 2) return launch_np_p<14, 2>(c, a, s);
+  if (c.P == 16 && c.T == 2) return launch_np_p<16, 2>(c, a, s);
+  if (c.P == 16 && c.T == 1) return launch_np_p<16, 1>(c, a, s);
   const size_t smem = np_smem_bytes(c.P, c.T, c.K, a.nwr);
   cudaError_t e = cudaFuncSetAttribute(normalize_patchify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);

@@ -32,7 +32,13 @@ struct Ctx {
   int kint = 0;        // T * kslice_pad (internal weight row width)
   __nv_bfloat16* w_int = nullptr;  // [N][kint]: column s*kslice_pad + (ph*P + pw)*3 + c
   float* bias = nullptr;           // [N] fp32 (zeros when no bias)
-  float* rope_tab = nullptr;       // scratch: cos/sin axis table [2][VITFE_ROPE_MAX_SIDE][HD/4]
+  // RoPE axis tables (the cos/sin cache), one slot per (head_dim, theta) seen, each
+  // [2][VITFE_ROPE_MAX_SIDE][head_dim/4] fp32 covering every position, built on first use
+  static constexpr int kRopeSlots = 4;
+  float* rope_tab = nullptr;       // kRopeSlots x slot_floats
+  int rope_hd[kRopeSlots] = {0, 0, 0, 0};
+  float rope_theta[kRopeSlots] = {0.f, 0.f, 0.f, 0.f};
+  int rope_next = 0;               // slot replaced next when all are taken
   CUtensorMap tmap_w;              // 2-D map over w_int, box {64, bn/2}, 128-byte swizzle
   int bn = 0;                      // GEMM N tile of a CTA pair (<= 256)
   int nstage = 0;                  // B pipeline stages
@@ -448,7 +454,7 @@ cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_byte
                          const vitfe_item* items, const int32_t* n_items, int max_items,
                          int64_t rows, void* out, int32_t* status, cudaStream_t s);
 cudaError_t embed_configure(Ctx& c);
-cudaError_t launch_rope(const Ctx& c, const vitfe_item* items, const int32_t* n_items,
+cudaError_t launch_rope(Ctx& c, const vitfe_item* items, const int32_t* n_items,
                         int max_items, int64_t rows, int head_dim, float theta, float* cos,
                         float* sin, int32_t* status, cudaStream_t s);
 cudaError_t launch_normalize_patchify(const Ctx& c, const uint8_t* pixels, int64_t pixel_bytes,
