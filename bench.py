@@ -388,7 +388,9 @@ def main():
                        "normalize_patchify_frac_hbm": np_bytes / (np_ms / 1e3) / 1e9 / float(pk["hbm_gbs"])},
         "e2e": {"value": world * rows / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 3 * args.steps,
+        # per step: embed_kernel + rope_expand_kernel (the position table stays cached
+        # in the handle after the warm-up steps built it)
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
