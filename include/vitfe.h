@@ -111,7 +111,12 @@ vitfe_status vitfe_embed(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes,
  * cos[r] = [cos(hpos*w_i)]_i || [cos(wpos*w_i)]_i, sin likewise.
  * cos, sin: device float32 [rows][head_dim/2], 16-byte aligned.
  * head_dim % 8 == 0, 8 <= head_dim <= VITFE_ROPE_MAX_HEAD_DIM; theta > 0.
- * Items with h or w > VITFE_ROPE_MAX_SIDE are rejected on the device. */
+ * Items with h or w > VITFE_ROPE_MAX_SIDE are rejected on the device.
+ * The handle builds the axis table of a (head_dim, theta) pair once, over every
+ * position below VITFE_ROPE_MAX_SIDE, and keeps it for its lifetime; it keeps up
+ * to 4 pairs, and a call with a further pair rebuilds a transient table each time.
+ * A table first needed inside a stream capture is built by the graph on every
+ * replay; one eager call before the capture keeps that build out of the graph. */
 vitfe_status vitfe_rope(vitfe_t h, const vitfe_item* items, const int32_t* n_items,
                         int32_t max_items, int64_t rows, int head_dim, float theta,
                         float* cos, float* sin, int32_t* status, cudaStream_t stream);

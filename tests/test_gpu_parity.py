@@ -305,3 +305,59 @@ def test_graph_replay_bucket_masks_pad_rows():
         rc, _ = oracle.rope_workload(sub)
         assert np.max(np.abs(c[:live] - rc)) <= U.ROPE_MAX_ABS
     fe.close()
+
+
+def _rope_check(fe, b, wl, head_dim, theta, rows, cos=None, sin=None):
+    c, s_ = (cos, sin) if cos is not None else fe.rope(b, head_dim, theta, rows=rows)
+    torch.cuda.synchronize()
+    rc, rs = oracle.rope_workload(wl, bucket_rows=rows, head_dim=head_dim, theta=theta)
+    assert np.max(np.abs(c.cpu().numpy() - rc)) <= U.ROPE_MAX_ABS
+    assert np.max(np.abs(s_.cpu().numpy() - rs)) <= U.ROPE_MAX_ABS
+
+
+def test_rope_table_first_built_inside_a_capture():
+    # the first call of a (head_dim, theta) pair is captured, not run: an eager call made
+    # before any replay must still build and use the right table, and the graph must
+    # build its own on replay
+    wl = synth.small_workload(9, [(1, 4, 6, 1), (2, 2, 4, 4)], patch=14, hidden=256, head_dim=80)
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    from vit_vision_encoder_fusedinputnorm_gb300 import binding as B
+    rows = b.live_rows + 12
+    cos = torch.full((rows, 40), 7.0, device="cuda")
+    sin = torch.full((rows, 40), 7.0, device="cuda")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        B.vitfe_rope(fe.h, b.items, b.n_items, b.capacity, rows, 80, wl.theta, cos, sin, None, s)
+    _rope_check(fe, b, wl, 80, wl.theta, rows)
+    cos.fill_(7.0)
+    sin.fill_(7.0)
+    g.replay()
+    _rope_check(fe, b, wl, 80, wl.theta, rows, cos, sin)
+    fe.close()
+
+
+def test_rope_tables_beyond_the_cached_slots_and_graph_reading_a_slot():
+    # a graph captured on a cached pair keeps reading that pair's table after many other
+    # pairs (more than the handle caches) have been used eagerly
+    wl = synth.small_workload(11, [(1, 6, 4, 1), (1, 2, 2, 1)], patch=14, hidden=256, head_dim=80)
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    from vit_vision_encoder_fusedinputnorm_gb300 import binding as B
+    rows = b.live_rows
+    _rope_check(fe, b, wl, 80, 10000.0, rows)
+    cos = torch.empty((rows, 40), device="cuda")
+    sin = torch.empty((rows, 40), device="cuda")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        B.vitfe_rope(fe.h, b.items, b.n_items, b.capacity, rows, 80, 10000.0, cos, sin, None, s)
+    for hd, th in [(64, 10000.0), (80, 500.0), (72, 10000.0), (80, 1e6), (96, 10000.0), (80, 123.0), (64, 10000.0)]:
+        _rope_check(fe, b, wl, hd, th, rows)
+    cos.fill_(7.0)
+    sin.fill_(7.0)
+    g.replay()
+    _rope_check(fe, b, wl, 80, 10000.0, rows, cos, sin)
+    _rope_check(fe, b, wl, 80, 123.0, rows)
+    fe.close()

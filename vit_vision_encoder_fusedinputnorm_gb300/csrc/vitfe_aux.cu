@@ -569,23 +569,27 @@ cudaError_t launch_rope(Ctx& c, const vitfe_item* items, const int32_t* n_items,
                         int head_dim, float theta, float* cos, float* sin, int32_t* status, cudaStream_t s) {
   const int nf = head_dim / 4;
   const size_t slot_floats = (size_t)2 * VITFE_ROPE_MAX_SIDE * (VITFE_ROPE_MAX_HEAD_DIM / 4);
-  // the cos/sin cache of this (head_dim, theta): built once over every position, then reused
+  // the cos/sin table of this (head_dim, theta): built once over every position, then reused
   int slot = -1;
-  for (int k = 0; k < Ctx::kRopeSlots; ++k)
+  for (int k = 0; k < c.rope_used; ++k)
     if (c.rope_hd[k] == head_dim && c.rope_theta[k] == theta) slot = k;
-  float* tab;
-  if (slot < 0) {
-    slot = c.rope_next;
-    c.rope_next = (c.rope_next + 1) % Ctx::kRopeSlots;
-    tab = c.rope_tab + (size_t)slot * slot_floats;
-    rope_cache_kernel<<<grid_for((long long)VITFE_ROPE_MAX_SIDE * nf, kAuxThreads, c.sm_count * 4), kAuxThreads, 0,
-                        s>>>(nf, (double)theta, tab);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+  if (slot < 0 && c.rope_used < Ctx::kRopeSlots) {
+    slot = c.rope_used++;
     c.rope_hd[slot] = head_dim;
     c.rope_theta[slot] = theta;
-  } else {
-    tab = c.rope_tab + (size_t)slot * slot_floats;
+    c.rope_built[slot] = false;
+  }
+  const bool transient = slot < 0;
+  float* tab = c.rope_tab + (size_t)(transient ? Ctx::kRopeSlots : slot) * slot_floats;
+  if (transient || !c.rope_built[slot]) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return e;
+    rope_cache_kernel<<<grid_for((long long)VITFE_ROPE_MAX_SIDE * nf, kAuxThreads, c.sm_count * 4), kAuxThreads, 0,
+                        s>>>(nf, (double)theta, tab);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (!transient && cap == cudaStreamCaptureStatusNone) c.rope_built[slot] = true;
   }
   const int grid = grid_for(rows, kAuxThreads, c.sm_count * 16);   // 8 warps x 32 rows per CTA
   rope_expand_kernel<<<grid, kAuxThreads, 0, s>>>(items, n_items, max_items, c.T, c.M, (int)rows, nf, tab, cos, sin,

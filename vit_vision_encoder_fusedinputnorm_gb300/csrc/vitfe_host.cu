@@ -114,7 +114,7 @@ vitfe_status vitfe_create(vitfe_t* out, const float mean[3], const float std_[3]
 
   if (cudaMalloc(&c.w_int, (size_t)c.N * c.kint * sizeof(__nv_bfloat16)) != cudaSuccess ||
       cudaMalloc(&c.bias, (size_t)c.N * sizeof(float)) != cudaSuccess ||
-      cudaMalloc(&c.rope_tab, (size_t)vitfe::Ctx::kRopeSlots * 2 * VITFE_ROPE_MAX_SIDE * (VITFE_ROPE_MAX_HEAD_DIM / 4) *
+      cudaMalloc(&c.rope_tab, (size_t)(vitfe::Ctx::kRopeSlots + 1) * 2 * VITFE_ROPE_MAX_SIDE * (VITFE_ROPE_MAX_HEAD_DIM / 4) *
                                   sizeof(float)) !=
           cudaSuccess) {
     cudaGetLastError();

@@ -35,10 +35,17 @@ struct Ctx {
   // RoPE axis tables (the cos/sin cache), one slot per (head_dim, theta) seen, each
   // [2][VITFE_ROPE_MAX_SIDE][head_dim/4] fp32 covering every position, built on first use
   static constexpr int kRopeSlots = 4;
-  float* rope_tab = nullptr;       // kRopeSlots x slot_floats
+  // RoPE axis tables: kRopeSlots cached tables, each keyed by (head_dim, theta) for the
+  // handle's lifetime (a slot is never given to another key, so a captured graph that
+  // reads a slot stays valid), plus one transient slot rebuilt by every call whose key
+  // found no slot.  rope_built[k]: an eager build of slot k has been enqueued.  A build
+  // recorded during stream capture runs only when the graph does, so it leaves the slot
+  // unbuilt for eager calls.
+  float* rope_tab = nullptr;       // (kRopeSlots + 1) x slot_floats
   int rope_hd[kRopeSlots] = {0, 0, 0, 0};
   float rope_theta[kRopeSlots] = {0.f, 0.f, 0.f, 0.f};
-  int rope_next = 0;               // slot replaced next when all are taken
+  bool rope_built[kRopeSlots] = {false, false, false, false};
+  int rope_used = 0;               // slots holding a key
   CUtensorMap tmap_w;              // 2-D map over w_int, box {64, bn/2}, 128-byte swizzle
   int bn = 0;                      // GEMM N tile of a CTA pair (<= 256)
   int nstage = 0;                  // B pipeline stages
