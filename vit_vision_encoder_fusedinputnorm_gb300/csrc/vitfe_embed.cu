@@ -458,10 +458,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kMmaWarp) {
-    if (lane == 0 && leader) {
-      // The single issuing thread is the throughput limiter (each tcgen05.mma issue costs
-      // it tens of cycles), so the code between issues is minimal: descriptors at
-      // constant offsets, a one-instruction fast path for barriers already complete.
+    if (leader) {
+      // The whole warp runs the issue loop, so its indices and descriptors stay warp-uniform
+      // (uniform registers); one elected lane issues each group of MMAs and its commit.
+      // Issue throughput of this one warp bounds the kernel, so the code between issues is
+      // minimal: descriptors at constant offsets, one poll and vote for barriers already
+      // complete.
       uint32_t na = 0, np = 0, stage = 0, bphase = 0;
       bool ok = true;
       const uint64_t adesc0 = sw128_desc(a_smem);
@@ -477,24 +479,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 #define VITFE_WAIT_B()                                                                        \
   do {                                                                                        \
-    const uint32_t bar_ = b_full0 + 8u * stage;                                               \
-    if (!mbar_try_wait(bar_, bphase) && !mbar_wait(bar_, bphase, abort_flag, args.limit_ns))  \
-      ok = false;                                                                             \
+    if (!mbar_wait_warp<false>(b_full0 + 8u * stage, bphase, abort_flag, args.limit_ns)) ok = false; \
   } while (0)
 #define VITFE_WAIT_A(J)                                                                       \
   do {                                                                                        \
-    const uint32_t abar_ = a_full0 + 8u * (J);                                                \
-    if (!mbar_try_wait_cluster(abar_, np & 1u) && !mbar_wait_cl(abar_, np & 1u, abort_flag, args.limit_ns)) \
-      ok = false;                                                                             \
+    if (!mbar_wait_warp<true>(a_full0 + 8u * (J), np & 1u, abort_flag, args.limit_ns)) ok = false; \
   } while (0)
 #define VITFE_STEP(ADESC, NK, FIRST)                                                          \
   do {                                                                                        \
     const uint64_t bd_ = bd_cur;                                                              \
-    umma_bf16_pair(d_tmem, (ADESC), bd_, idesc, (FIRST) ? 0u : 1u);                           \
-    if ((NK) > 1) umma_bf16_pair(d_tmem, (ADESC) + 2u, bd_ + 2u, idesc, 1u);                 \
-    if ((NK) > 2) umma_bf16_pair(d_tmem, (ADESC) + 4u, bd_ + 4u, idesc, 1u);                 \
-    if ((NK) > 3) umma_bf16_pair(d_tmem, (ADESC) + 6u, bd_ + 6u, idesc, 1u);                 \
-    umma_commit_pair(b_empty0 + 8u * stage);                                                  \
+    if (elect_one()) {                                                                        \
+      umma_bf16_pair(d_tmem, (ADESC), bd_, idesc, (FIRST) ? 0u : 1u);                         \
+      if ((NK) > 1) umma_bf16_pair(d_tmem, (ADESC) + 2u, bd_ + 2u, idesc, 1u);               \
+      if ((NK) > 2) umma_bf16_pair(d_tmem, (ADESC) + 4u, bd_ + 4u, idesc, 1u);               \
+      if ((NK) > 3) umma_bf16_pair(d_tmem, (ADESC) + 6u, bd_ + 6u, idesc, 1u);               \
+      umma_commit_pair(b_empty0 + 8u * stage);                                                \
+    }                                                                                         \
+    __syncwarp();                                                                             \
     if (++stage == nstage) {                                                                  \
       stage = 0;                                                                              \
       bphase ^= 1u;                                                                           \
@@ -509,7 +510,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (kind == kPad) continue;
         for (int p = 0; ok && p < args.npass; ++p) {
           const uint32_t buf = na & 1u;
-          if (!mbar_wait_cl(smem_u32(&hs->acc_empty[buf]), ((na >> 1) & 1u) ^ 1u, abort_flag, args.limit_ns)) {
+          if (!mbar_wait_warp<true>(smem_u32(&hs->acc_empty[buf]), ((na >> 1) & 1u) ^ 1u, abort_flag, args.limit_ns)) {
             ok = false;
             break;
           }
@@ -529,7 +530,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 VITFE_STEP(ad, ksteps_of<P>(j), j == 0 && sl == 0);
               }
               if (!ok) break;
-              if (p == args.npass - 1) umma_commit_pair(a_empty0 + 8u * j);
+              if (p == args.npass - 1) {
+                if (elect_one()) umma_commit_pair(a_empty0 + 8u * j);
+                __syncwarp();
+              }
             }
           } else {
             for (int sl = 0; ok && sl < T; ++sl) {
@@ -539,13 +543,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 VITFE_WAIT_B();
                 if (!ok) break;
                 VITFE_STEP(adesc0 + (uint64_t)(j * (kABlockBytes >> 4)), ksteps_of<P>(j), sl == 0 && j == 0);
-                umma_commit_pair(a_empty0 + 8u * j);
+                if (elect_one()) umma_commit_pair(a_empty0 + 8u * j);
+                __syncwarp();
               }
               ++np;   // one slice production consumed
             }
           }
           if (!ok) break;
-          umma_commit_pair(smem_u32(&hs->acc_full[buf]));
+          if (elect_one()) umma_commit_pair(smem_u32(&hs->acc_full[buf]));
+          __syncwarp();
           ++na;
         }
         if (kind == kResident) ++np;
@@ -554,7 +560,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #undef VITFE_WAIT_A
 #undef VITFE_WAIT_B
       if (!ok) {
-        umma_commit_pair(smem_u32(&hs->drain));
+        // the elected lane issued every MMA: its commit covers them all
+        if (elect_one()) umma_commit_pair(smem_u32(&hs->drain));
+        __syncwarp();
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait_cluster(smem_u32(&hs->drain), 0u) && global_timer_ns() - t0 < args.limit_ns) {
         }

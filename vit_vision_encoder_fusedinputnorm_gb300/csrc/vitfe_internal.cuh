@@ -443,6 +443,43 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, 
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// One lane of a converged warp is elected (the same lane every time for a full warp).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(p));
+  return p != 0;
+}
+
+// Bounded mbarrier wait by a whole converged warp (acquire at CTA or cluster scope).  The
+// lanes vote on every poll, so they all return together and with the same value: true when
+// the phase of `parity` has completed, false (and *abort_flag set) when the abort flag was
+// raised or `limit_ns` passed first.
+template <bool kCluster>
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
+  if constexpr (kCluster) return mbar_try_wait_cluster(bar, parity);
+  else return mbar_try_wait(bar, parity);
+}
+template <bool kCluster>
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               uint64_t limit_ns) {
+  if (__all_sync(0xffffffffu, mbar_poll<kCluster>(bar, parity))) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (__all_sync(0xffffffffu, mbar_poll<kCluster>(bar, parity))) return true;
+    if ((i & 15u) == 0) {
+      const bool stop = *abort_flag != 0 || global_timer_ns() - t0 > limit_ns;
+      if (__any_sync(0xffffffffu, stop)) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Arrive once on the barrier at offset `bar` in both CTAs of the pair when all prior
 // tcgen05 ops of this thread complete.
 __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
