@@ -525,35 +525,50 @@ size_t np_smem_bytes(int P, int T, int K, int nwr) {
 }
 
 // ---------------------------------------------------------------------------
-// create-time weight permutation: canonical (C, T, P, P) columns -> internal
-// [slice t][(ph, pw, c)] columns, each slice zero-padded to kslice_pad.
+// Create-time weight tiling.  The embed kernel reads W as whole shared-memory images:
+// block (pass p, CTA half r, temporal slice s, K block j) holds the bnh = bn/2 weight
+// rows n = p*bn + r*(npw/2) + i (i < npw/2, npw = min(bn, N - p*bn); other rows zero)
+// times the 64 internal features 64*j + e of slice s, in the 128-byte-swizzled K-major
+// layout the MMA descriptor expects: row i at i*128, 16-byte chunk q of the row at
+// chunk position q ^ (i & 7).  Internal feature kp of a slice is (ph*P + pw)*3 + c
+// (zero past 3*P*P); it holds canonical column ((c*T + s)*P + ph)*P + pw.
 // ---------------------------------------------------------------------------
-__global__ void permute_weight_kernel(const __nv_bfloat16* __restrict__ W, const __nv_bfloat16* __restrict__ b,
-                                      int N, int P, int T, int kslice, int kslice_pad,
-                                      __nv_bfloat16* __restrict__ w_int, float* __restrict__ bias) {
-  const int kint = T * kslice_pad;
+__global__ void tile_weight_kernel(const __nv_bfloat16* __restrict__ W, const __nv_bfloat16* __restrict__ b,
+                                   int N, int P, int T, int nblk, int bn,
+                                   __nv_bfloat16* __restrict__ w_tile, float* __restrict__ bias) {
+  const int kslice = 3 * P * P;
   const int K = T * kslice;
-  const long long total = (long long)N * kint;
+  const int bnh = bn / 2;
+  const int npass = (N + bn - 1) / bn;
+  const long long per_blk = (long long)bnh * 64;
+  const long long total = (long long)npass * 2 * T * nblk * per_blk;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
-    const int n = (int)(idx / kint);
-    const int col = (int)(idx - (long long)n * kint);
-    const int s = col / kslice_pad;
-    const int kp = col - s * kslice_pad;
+    const long long blk = idx / per_blk;
+    const int within = (int)(idx - blk * per_blk);
+    const int i = within >> 6;
+    const int qp = (within >> 3) & 7;                 // physical chunk in the row
+    const int e = ((qp ^ (i & 7)) << 3) | (within & 7);
+    const int j = (int)(blk % nblk);
+    const int sl = (int)((blk / nblk) % T);
+    const int r = (int)((blk / ((long long)nblk * T)) & 1);
+    const int p = (int)(blk / ((long long)nblk * T * 2));
+    const int npw = min(bn, N - p * bn);
+    const int kp = 64 * j + e;
     __nv_bfloat16 v = __float2bfloat16_rn(0.0f);
-    if (kp < kslice) {
+    if (i < npw / 2 && kp < kslice) {
+      const int n = p * bn + r * (npw / 2) + i;
       const int ph = kp / (3 * P);
       const int rem = kp - ph * 3 * P;
       const int pw = rem / 3;
       const int c = rem - pw * 3;
-      const int k = ((c * T + s) * P + ph) * P + pw;
-      v = W[(size_t)n * K + k];
+      v = W[(size_t)n * K + ((c * T + sl) * P + ph) * P + pw];
     }
-    w_int[idx] = v;
-    if (col == 0) bias[n] = b ? __bfloat162float(b[n]) : 0.0f;
+    w_tile[idx] = v;
   }
+  for (long long n = (long long)blockIdx.x * blockDim.x + threadIdx.x; n < N; n += (long long)gridDim.x * blockDim.x)
+    bias[n] = b ? __bfloat162float(b[n]) : 0.0f;
 }
-
 
 }  // namespace
 
@@ -628,10 +643,10 @@ cudaError_t launch_normalize_patchify(const Ctx& c, const uint8_t* pixels, int64
   return cudaGetLastError();
 }
 
-cudaError_t launch_permute_weight(const Ctx& c, const __nv_bfloat16* W, const __nv_bfloat16* b, cudaStream_t s) {
-  const long long total = (long long)c.N * c.kint;
+cudaError_t launch_tile_weight(const Ctx& c, const __nv_bfloat16* W, const __nv_bfloat16* b, cudaStream_t s) {
+  const long long total = (long long)c.w_tile_bytes / 2;
   const int grid = grid_for(total, 256, c.sm_count * 16);
-  permute_weight_kernel<<<grid, 256, 0, s>>>(W, b, c.N, c.P, c.T, c.kslice, c.kslice_pad, c.w_int, c.bias);
+  tile_weight_kernel<<<grid, 256, 0, s>>>(W, b, c.N, c.P, c.T, c.nblk, c.bn, c.w_tile, c.bias);
   return cudaGetLastError();
 }
 

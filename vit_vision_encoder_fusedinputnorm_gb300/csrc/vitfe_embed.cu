@@ -13,7 +13,8 @@
 //               uint8 pixel runs with aligned 4-byte loads, normalise in fp32, round to
 //               bf16 and store into 128-byte-swizzled K-major shared-memory blocks (64
 //               features each);
-//   warp 12     TMA producer of this CTA's half of each W tile (box 64 x bn/2);
+//   warp 12     TMA producer of this CTA's half of each W tile: one box copies one
+//               shared-memory image of the pre-tiled weight (bn/8 rows of 512 bytes);
 //   warp 13     tensor-memory allocation (both CTAs); in the even CTA one thread issues
 //               the MMAs (fp32 accumulators double-buffered in tensor memory);
 //   warps 8-11  epilogue, one warp per tensor-memory lane quarter: tcgen05.ld of the
@@ -59,7 +60,6 @@ struct EmbedArgs {
   const float* bias;
   float scale0, scale1, scale2, shift0, shift1, shift2;
   int T, M, N;
-  int kslice_pad;
   int bn, nstage, npass;
   int tmem_cols;
   int num_tiles;   // 256-row pair tiles
@@ -420,9 +420,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (kind == kPad) continue;
         const int nsteps = args.T * NBLK;
         for (int p = 0; ok && p < args.npass; ++p) {
-          const int n0 = p * args.bn;
-          const int npw = min(args.bn, args.N - n0);
-          const int c1 = n0 + (int)rank * (npw / 2);
+          // this CTA's images of pass p: (p, rank, slice, block), bnh/4 rows of 512 B each
+          const int blk0 = (p * 2 + (int)rank) * args.T * NBLK;
           for (int st = 0; ok && st < nsteps; ++st) {
             const int j = (kind == kResident) ? st / args.T : st % NBLK;
             const int sl = (kind == kResident) ? st % args.T : st / NBLK;
@@ -431,8 +430,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               break;
             }
             if (leader) mbar_arrive_expect_tx(smem_u32(&hs->b_full[stage]), 2u * b_stage_bytes);
-            tma_load_2d_pair(b_smem + stage * b_stage_bytes, &tmap_w, b_full_L + 8u * stage,
-                             sl * args.kslice_pad + 64 * j, c1);
+            tma_load_2d_pair(b_smem + stage * b_stage_bytes, &tmap_w, b_full_L + 8u * stage, 0,
+                             (blk0 + sl * NBLK + j) * (bnh / 4));
             ++nb;
             if (++stage == (uint32_t)args.nstage) { stage = 0; bphase ^= 1u; }
           }
@@ -719,7 +718,6 @@ cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_byte
   a.T = c.T;
   a.M = c.M;
   a.N = c.N;
-  a.kslice_pad = c.kslice_pad;
   a.bn = c.bn;
   a.nstage = c.nstage;
   a.npass = (c.N + c.bn - 1) / c.bn;

@@ -36,7 +36,7 @@ constexpr int64_t kMaxRows = 0x7fffffffLL - 1024;
 
 void free_ctx(vitfe_ctx* h) {
   if (!h) return;
-  if (h->c.w_int) cudaFree(h->c.w_int);
+  if (h->c.w_tile) cudaFree(h->c.w_tile);
   if (h->c.bias) cudaFree(h->c.bias);
   if (h->c.rope_tab) cudaFree(h->c.rope_tab);
   delete h;
@@ -106,14 +106,12 @@ vitfe_status vitfe_create(vitfe_t* out, const float mean[3], const float std_[3]
   c.kslice_pad = (c.kslice + 63) / 64 * 64;
   c.nblk = c.kslice_pad / 64;
   c.K = tpatch * c.kslice;
-  c.kint = tpatch * c.kslice_pad;
   if (const char* env = std::getenv("VITFE_WAIT_LIMIT_MS")) {
     const long ms = std::strtol(env, nullptr, 10);
     if (ms > 0) c.wait_limit_ns = (uint64_t)ms * 1000000ull;
   }
 
-  if (cudaMalloc(&c.w_int, (size_t)c.N * c.kint * sizeof(__nv_bfloat16)) != cudaSuccess ||
-      cudaMalloc(&c.bias, (size_t)c.N * sizeof(float)) != cudaSuccess ||
+  if (cudaMalloc(&c.bias, (size_t)c.N * sizeof(float)) != cudaSuccess ||
       cudaMalloc(&c.rope_tab, (size_t)(vitfe::Ctx::kRopeSlots + 1) * 2 * VITFE_ROPE_MAX_SIDE * (VITFE_ROPE_MAX_HEAD_DIM / 4) *
                                   sizeof(float)) !=
           cudaSuccess) {
@@ -121,27 +119,40 @@ vitfe_status vitfe_create(vitfe_t* out, const float mean[3], const float std_[3]
     free_ctx(h);
     return VITFE_ENOMEM;
   }
-  cudaError_t e = vitfe::launch_permute_weight(c, static_cast<const __nv_bfloat16*>(W),
-                                               static_cast<const __nv_bfloat16*>(b), stream);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-  if (e == cudaSuccess) e = vitfe::embed_configure(c);
+  // the embed kernel's tile shape decides the weight layout
+  cudaError_t e = vitfe::embed_configure(c);
   if (e != cudaSuccess) {
     free_ctx(h);
     return VITFE_ECUDA;
   }
   if (c.embed_ok) {
+    const size_t npass = (size_t)((c.N + c.bn - 1) / c.bn);
+    c.w_tile_bytes = npass * 2 * (size_t)c.T * (size_t)c.nblk * (size_t)(c.bn / 2) * 128;
+    if (cudaMalloc(&c.w_tile, c.w_tile_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      free_ctx(h);
+      return VITFE_ENOMEM;
+    }
+    e = vitfe::launch_tile_weight(c, static_cast<const __nv_bfloat16*>(W), static_cast<const __nv_bfloat16*>(b),
+                                  stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+      free_ctx(h);
+      return VITFE_ECUDA;
+    }
     EncodeTiledFn enc = get_encode_tiled();
     if (enc == nullptr) {
       free_ctx(h);
       return VITFE_ECUDA;
     }
-    const cuuint64_t gdim[2] = {(cuuint64_t)c.kint, (cuuint64_t)c.N};
-    const cuuint64_t gstride[1] = {(cuuint64_t)c.kint * sizeof(__nv_bfloat16)};
-    // each CTA of a pair loads half of a tile's W rows
-    const cuuint32_t box[2] = {64u, (cuuint32_t)(c.bn / 2)};
+    // the tiled weight as rows of 512 bytes: one box (bn/8 rows) is one shared-memory image
+    const cuuint64_t rows512 = (cuuint64_t)(c.w_tile_bytes / 512);
+    const cuuint64_t gdim[2] = {256u, rows512};
+    const cuuint64_t gstride[1] = {512u};
+    const cuuint32_t box[2] = {256u, (cuuint32_t)(c.bn / 8)};
     const cuuint32_t estride[2] = {1u, 1u};
-    CUresult r = enc(&c.tmap_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.w_int, gdim, gstride, box, estride,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = enc(&c.tmap_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.w_tile, gdim, gstride, box, estride,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
       free_ctx(h);

@@ -29,8 +29,8 @@ struct Ctx {
   int kslice_pad = 0;  // kslice rounded up to 64 (one 128-byte swizzle row of bf16)
   int nblk = 0;        // kslice_pad / 64
   int K = 0;           // 3 * T * P * P (canonical feature width)
-  int kint = 0;        // T * kslice_pad (internal weight row width)
-  __nv_bfloat16* w_int = nullptr;  // [N][kint]: column s*kslice_pad + (ph*P + pw)*3 + c
+  __nv_bfloat16* w_tile = nullptr; // W as the embed kernel's shared-memory images (tile_weight_kernel)
+  size_t w_tile_bytes = 0;
   float* bias = nullptr;           // [N] fp32 (zeros when no bias)
   // RoPE axis tables (the cos/sin cache), one slot per (head_dim, theta) seen, each
   // [2][VITFE_ROPE_MAX_SIDE][head_dim/4] fp32 covering every position, built on first use
@@ -46,7 +46,7 @@ struct Ctx {
   float rope_theta[kRopeSlots] = {0.f, 0.f, 0.f, 0.f};
   bool rope_built[kRopeSlots] = {false, false, false, false};
   int rope_used = 0;               // slots holding a key
-  CUtensorMap tmap_w;              // 2-D map over w_int, box {64, bn/2}, 128-byte swizzle
+  CUtensorMap tmap_w;              // w_tile viewed as 512-byte rows; a box is one image (bn/8 rows)
   int bn = 0;                      // GEMM N tile of a CTA pair (<= 256)
   int nstage = 0;                  // B pipeline stages
   int max_clusters = 0;            // co-resident CTA pairs of the embed kernel
@@ -508,7 +508,7 @@ cudaError_t launch_normalize_patchify(const Ctx& c, const uint8_t* pixels, int64
 cudaError_t launch_pos_ids(const Ctx& c, const vitfe_item* items, const int32_t* n_items,
                            int max_items, int64_t rows, int32_t* pos, int32_t* status,
                            cudaStream_t s);
-cudaError_t launch_permute_weight(const Ctx& c, const __nv_bfloat16* W, const __nv_bfloat16* b,
+cudaError_t launch_tile_weight(const Ctx& c, const __nv_bfloat16* W, const __nv_bfloat16* b,
                                   cudaStream_t s);
 
 }  // namespace vitfe
