@@ -104,6 +104,16 @@ __host__ __device__ constexpr int ksteps_of(int j) {
   return rem >= 64 ? 4 : (rem + 15) / 16;
 }
 
+// Order in which the MMA consumes (and, in a tile's last pass, releases) the K blocks of
+// a slice: 0, NBLK/2, 1, NBLK/2 + 1, ...  The two producer threads of a row fill blocks
+// [0, NBLK/2) and [NBLK/2, NBLK) in parallel, so this order consumes both halves at the
+// pace they are filled, and frees both early for the next tile.
+template <int NBLK>
+__host__ __device__ constexpr int blk_order(int jj) {
+  static_assert(NBLK % 2 == 0, "two producer halves of equal size");
+  return (jj & 1) ? NBLK / 2 + jj / 2 : jj / 2;
+}
+
 // Two fp32 lanes in one 64-bit register (packed f32x2 arithmetic, exact per lane).
 __device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
   uint64_t r;
@@ -423,7 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // this CTA's images of pass p: (p, rank, slice, block), bnh/4 rows of 512 B each
           const int blk0 = (p * 2 + (int)rank) * args.T * NBLK;
           for (int st = 0; ok && st < nsteps; ++st) {
-            const int j = (kind == kResident) ? st / args.T : st % NBLK;
+            const int j = blk_order<NBLK>((kind == kResident) ? st / args.T : st % NBLK);
             const int sl = (kind == kResident) ? st % args.T : st / NBLK;
             if (!mbar_wait_cl(smem_u32(&hs->b_empty[stage]), bphase ^ 1u, abort_flag, args.limit_ns)) {
               ok = false;
@@ -520,7 +530,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (kind == kResident) {
             // one resident slice of A feeds every temporal slice of W
 #pragma unroll
-            for (int j = 0; j < NBLK; ++j) {
+            for (int jj = 0; jj < NBLK; ++jj) {
+              const int j = blk_order<NBLK>(jj);
               if (p == 0) VITFE_WAIT_A(j);
               const uint64_t ad = adesc0 + (uint64_t)(j * (kABlockBytes >> 4));
               for (int sl = 0; ok && sl < T; ++sl) {
@@ -537,7 +548,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           } else {
             for (int sl = 0; ok && sl < T; ++sl) {
 #pragma unroll
-              for (int j = 0; j < NBLK; ++j) {
+              for (int jj = 0; jj < NBLK; ++jj) {
+                const int j = blk_order<NBLK>(jj);
                 VITFE_WAIT_A(j);
                 VITFE_WAIT_B();
                 if (!ok) break;
