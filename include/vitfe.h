@@ -19,9 +19,9 @@
  *  - All tensors are caller-owned DEVICE memory unless a parameter says
  *    "host".  Nothing here allocates, frees, synchronises or copies between
  *    host and device except vitfe_create / vitfe_destroy, so vitfe_embed,
- *    vitfe_rope, vitfe_normalize_patchify and vitfe_pos_ids can be captured
- *    in a CUDA graph: per-call metadata (the item table and its count) is
- *    read on the device at run time.
+ *    vitfe_rope, vitfe_normalize_patchify, vitfe_pos_ids and vitfe_cu_seqlens
+ *    can be captured in a CUDA graph: per-call metadata (the item table and
+ *    its count) is read on the device at run time.
  *  - A handle serialises its own work: calls that share a handle must be
  *    ordered (one stream, or events between streams).
  *  - Host-side argument errors return a status and launch nothing.
@@ -134,6 +134,20 @@ vitfe_status vitfe_normalize_patchify(vitfe_t h, const uint8_t* pixels, int64_t 
 vitfe_status vitfe_pos_ids(vitfe_t h, const vitfe_item* items, const int32_t* n_items,
                            int32_t max_items, int64_t rows, int32_t* pos, int32_t* status,
                            cudaStream_t stream);
+
+/* Attention sequence boundaries ("vLLM 多模态推理｜ViT 性能优化" §3.4): the
+ * encoder's attention keeps images apart, and its variable-length kernels take
+ * the first row of every sequence.  Each temporal group of an item (a still: the
+ * image) is one sequence of h*w rows, in item order, clipped to `rows`.
+ * cu_seqlens (device int32 [max_seqs + 1]): cu_seqlens[0] = 0, cu_seqlens[s + 1]
+ *   = end row of sequence s; entries past the last sequence repeat its end.
+ * seq_info (device int32 [2]): {number of sequences, longest sequence}.
+ * More than max_seqs sequences: the first max_seqs are written and the status
+ * word reports VITFE_EDEVICE_RANGE.  One small launch; capturable. */
+vitfe_status vitfe_cu_seqlens(vitfe_t h, const vitfe_item* items, const int32_t* n_items,
+                              int32_t max_items, int64_t rows, int32_t max_seqs,
+                              int32_t* cu_seqlens, int32_t* seq_info, int32_t* status,
+                              cudaStream_t stream);
 
 /* Allocation-free 2D-RoPE tables, for callers that cannot allocate device memory:
  * code under a memory pool it does not own, inside a CUDA-graph capture that must

@@ -45,7 +45,8 @@ import numpy as np
 __all__ = [
     "bf16_bits_to_f64", "normalize", "patchify", "normalize_patchify_item",
     "embed_rows", "embed_item", "embed_workload", "pos_ids", "rope_tables",
-    "rope_workload", "pos_ids_workload", "normalize_patchify_workload",
+    "rope_workload", "pos_ids_workload", "normalize_patchify_workload", "cu_seqlens",
+    "cu_seqlens_workload",
     "patch_coords",
 ]
 
@@ -204,6 +205,30 @@ def normalize_patchify_workload(wl, items=None, bucket_rows=None) -> np.ndarray:
             it.pixels, it.t, it.h, it.w, patch=wl.patch, tpatch=wl.tpatch, merge=wl.merge,
             mean=wl.mean, std=wl.std, rescale=wl.rescale)
     return out
+
+
+# ---------------------------------------------------------------------------
+# 3b. attention sequence boundaries
+# ---------------------------------------------------------------------------
+
+def cu_seqlens(grids: Sequence[Tuple[int, int, int]]) -> Tuple[np.ndarray, int]:
+    """(cu_seqlens int64 [n_seq + 1], longest sequence) of items with grids (t, h, w).
+
+    "vLLM 多模态推理｜ViT 性能优化", §3.4: cu_seqlens records where each image's
+    tokens start and end, so the encoder's attention keeps images apart.  The
+    encoder models single images and single frames (§3.3), so each of an item's
+    t temporal groups is one sequence of h*w tokens, in item order.
+    """
+    lens = []
+    for t, h, w in grids:
+        lens.extend([h * w] * t)
+    cu = np.concatenate([[0], np.cumsum(np.asarray(lens, dtype=np.int64))]).astype(np.int64)
+    return cu, (max(lens) if lens else 0)
+
+
+def cu_seqlens_workload(wl, items=None) -> Tuple[np.ndarray, int]:
+    idx = list(range(len(wl.items))) if items is None else list(items)
+    return cu_seqlens([(wl.items[i].t, wl.items[i].h, wl.items[i].w) for i in idx])
 
 
 # ---------------------------------------------------------------------------

@@ -361,3 +361,45 @@ def test_rope_tables_beyond_the_cached_slots_and_graph_reading_a_slot():
     _rope_check(fe, b, wl, 80, 10000.0, rows, cos, sin)
     _rope_check(fe, b, wl, 80, 123.0, rows)
     fe.close()
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_cu_seqlens_vs_oracle(name):
+    P, N, grids = SMALL[name]
+    wl = synth.small_workload(3, grids, patch=P, hidden=N)
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    cu_ref, mx_ref = oracle.cu_seqlens_workload(wl)
+    nseq = len(cu_ref) - 1
+    st = fe.status_tensor()
+    for pad in (0, 37):
+        cap = nseq + 5
+        cu, info = fe.cu_seqlens(b, cap, rows=b.live_rows + pad, status=st)
+        torch.cuda.synchronize()
+        assert st.cpu().tolist() == [0, -1]
+        expect = np.concatenate([cu_ref, np.full(cap - nseq, cu_ref[-1])])
+        assert np.array_equal(cu.cpu().numpy(), expect)
+        assert info.cpu().tolist() == [nseq, mx_ref]
+    fe.close()
+
+
+def test_cu_seqlens_bucket_clipping_and_overflow():
+    # rows below the live rows clip the last sequences; more sequences than slots fill the
+    # slots and report VITFE_EDEVICE_RANGE
+    wl = synth.small_workload(4, [(1, 4, 4, 1), (3, 2, 4, 6), (1, 2, 2, 1)], patch=14, hidden=256)
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    cu_ref, _ = oracle.cu_seqlens_workload(wl)         # [0, 16, 24, 32, 40, 44]
+    st = fe.status_tensor()
+    cu, info = fe.cu_seqlens(b, 8, rows=28, status=st)
+    torch.cuda.synchronize()
+    # item 1 keeps rows [16, 28): its groups [16, 24) and [24, 28); item 2 starts past the bucket
+    assert cu_ref.tolist() == [0, 16, 24, 32, 40, 44]
+    assert cu.cpu().numpy().tolist() == [0, 16, 24, 28, 28, 28, 28, 28, 28]
+    assert info.cpu().tolist() == [3, 16]      # item 0 is the longest sequence
+    assert st.cpu().tolist() == [5, 1]        # item 1 is the first that overflows the bucket
+    cu, info = fe.cu_seqlens(b, 3, status=st)
+    torch.cuda.synchronize()
+    assert cu.cpu().numpy().tolist() == cu_ref[:4].tolist()
+    assert int(info[0]) == 3 and st.cpu().tolist() == [5, -1]
+    fe.close()

@@ -303,6 +303,27 @@ def test_pos_ids_agree_with_patch_coords():
     assert np.array_equal(oracle.pos_ids(3, 4, 6, 2), c[:, 1:])
 
 
+# ---------------------------------------------------------------- cu_seqlens
+
+def test_cu_seqlens_boundaries_are_where_item_or_frame_group_changes():
+    # independent construction: label every row of the packed items with (item, temporal
+    # group) from the patch order itself, then take the rows where the label changes
+    grids = [(1, 4, 6), (3, 2, 4), (1, 2, 2), (2, 6, 2)]
+    labels = np.concatenate([np.stack([np.full(t * h * w, i), oracle.patch_coords(t, h, w, 2)[:, 0]], 1)
+                             for i, (t, h, w) in enumerate(grids)])
+    change = np.flatnonzero(np.any(labels[1:] != labels[:-1], axis=1)) + 1
+    expect = np.concatenate([[0], change, [len(labels)]])
+    cu, mx = oracle.cu_seqlens(grids)
+    assert np.array_equal(cu, expect)
+    assert mx == int(np.max(np.diff(expect)))
+
+
+def test_cu_seqlens_stills_are_one_sequence_per_image():
+    cu, mx = oracle.cu_seqlens([(1, 16, 16), (1, 4, 6), (1, 96, 96)])
+    assert cu.tolist() == [0, 256, 280, 280 + 9216] and mx == 9216
+    assert oracle.cu_seqlens([])[0].tolist() == [0]
+
+
 # ---------------------------------------------------------------- RoPE
 
 def test_rope_position_zero_is_identity():

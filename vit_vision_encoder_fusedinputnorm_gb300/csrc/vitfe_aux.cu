@@ -49,6 +49,83 @@ __global__ void __launch_bounds__(kAuxThreads) pos_ids_kernel(const vitfe_item* 
 }
 
 // ---------------------------------------------------------------------------
+// Attention sequence boundaries ("vLLM 多模态推理｜ViT 性能优化" §3.4): the encoder's
+// attention keeps each image apart, so its varlen kernels take the first row of every
+// sequence.  The encoder sees single images and single frames (§3.3), so each temporal
+// group of an item is one sequence of h*w rows: cu[0] = 0 and, item by item and group by
+// group, cu[s + 1] = cu[s] + h*w, clipped to the bucket (a sequence past it is dropped).
+// Entries past the last sequence, up to max_seqs, repeat the last boundary; info =
+// {number of sequences, longest sequence}.  More than max_seqs sequences: the first
+// max_seqs are written and the status word reports VITFE_EDEVICE_RANGE.
+// One CTA: warp 0 builds the item table, the CTA scans the items' sequence counts.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kAuxThreads) cu_seqlens_kernel(const vitfe_item* items, const int32_t* n_items,
+                                                                 int max_items, int T, int M, int rows,
+                                                                 int max_seqs, int32_t* cu, int32_t* info,
+                                                                 int32_t* status) {
+  __shared__ SmemTab st;
+  __shared__ int sbase[kMaxItems + 1];    // first sequence of each item
+  __shared__ int smax[kAuxThreads / 32];
+  if (threadIdx.x < 32)
+    build_item_table(items, n_items, max_items, -1, 1, T, M, rows, 0x7fffffff, st.tab());
+  __syncthreads();
+  const int n = st.hdr.n;
+  // sequences of item i: its temporal groups whose rows start inside the bucket
+  auto nseq_of = [&](int i) -> int {
+    const int hw = items[i].h * items[i].w;
+    const int r0 = st.start[i], r1 = st.start[i + 1];
+    if (hw <= 0 || r1 <= r0) return 0;
+    return (r1 - r0 + hw - 1) / hw;
+  };
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int i = 0; i < n; ++i) {
+      sbase[i] = acc;
+      acc += nseq_of(i);
+    }
+    sbase[n] = acc;
+  }
+  __syncthreads();
+  const int total = sbase[n];
+  const int nw = min(total, max_seqs);
+  int mx = 0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int hw = items[i].h * items[i].w;
+    const int k = nseq_of(i);
+    for (int g = 0; g < k; ++g) {
+      const int sidx = sbase[i] + g;
+      const int end = min(st.start[i] + (g + 1) * hw, st.start[i + 1]);
+      mx = max(mx, end - (st.start[i] + g * hw));
+      if (sidx < nw) cu[sidx + 1] = end;
+    }
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+  if ((threadIdx.x & 31) == 0) smax[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  // pad: entries past the last boundary repeat it (only when every sequence fitted, so the
+  // last boundary is the end of the live rows)
+  const int last = (nw == 0) ? 0 : st.hdr.live;
+  for (int k = nw + 1 + threadIdx.x; k <= max_seqs; k += blockDim.x) cu[k] = last;
+  if (threadIdx.x == 0) {
+    cu[0] = 0;
+    int m = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = max(m, smax[w]);
+    info[0] = nw;
+    info[1] = m;
+    if (status != nullptr) {
+      if (st.hdr.code == kOk && total > max_seqs) {
+        status[0] = kRange;
+        status[1] = -1;
+      } else {
+        status[0] = st.hdr.code;
+        status[1] = st.hdr.bad_item;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // 2D-RoPE ("vLLM 多模态推理｜ViT 性能优化" §3.3 steps 1, 3, 5)
 // ---------------------------------------------------------------------------
 __device__ void rope_fill(float* tab, int nf, double theta, int maxside);
@@ -577,6 +654,14 @@ cudaError_t launch_pos_ids(const Ctx& c, const vitfe_item* items, const int32_t*
   const int grid = grid_for(rows, kAuxThreads, c.sm_count * 8);
   pos_ids_kernel<<<grid, kAuxThreads, 0, s>>>(items, n_items, max_items, c.T, c.M, (int)rows,
                                                reinterpret_cast<int2*>(pos), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cu_seqlens(const Ctx& c, const vitfe_item* items, const int32_t* n_items, int max_items,
+                              int64_t rows, int max_seqs, int32_t* cu, int32_t* info, int32_t* status,
+                              cudaStream_t s) {
+  cu_seqlens_kernel<<<1, kAuxThreads, 0, s>>>(items, n_items, max_items, c.T, c.M, (int)rows, max_seqs, cu, info,
+                                              status);
   return cudaGetLastError();
 }
 

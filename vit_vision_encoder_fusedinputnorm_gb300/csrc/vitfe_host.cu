@@ -217,6 +217,19 @@ vitfe_status vitfe_pos_ids(vitfe_t h, const vitfe_item* items, const int32_t* n_
   return from_cuda(vitfe::launch_pos_ids(h->c, items, n_items, max_items, rows, pos, status, stream));
 }
 
+vitfe_status vitfe_cu_seqlens(vitfe_t h, const vitfe_item* items, const int32_t* n_items, int32_t max_items,
+                              int64_t rows, int32_t max_seqs, int32_t* cu_seqlens, int32_t* seq_info,
+                              int32_t* status, cudaStream_t stream) {
+  vitfe_status st = check_common(h, items, n_items, max_items, rows);
+  if (st != VITFE_OK) return st;
+  if (max_seqs < 0 || max_seqs > kMaxRows) return VITFE_EINVAL;
+  if (cu_seqlens == nullptr || seq_info == nullptr || !aligned(cu_seqlens, 4) || !aligned(seq_info, 4))
+    return VITFE_EINVAL;
+  if (status && !aligned(status, 4)) return VITFE_EINVAL;
+  return from_cuda(vitfe::launch_cu_seqlens(h->c, items, n_items, max_items, rows, max_seqs, cu_seqlens, seq_info,
+                                            status, stream));
+}
+
 vitfe_status vitfe_items_from_grid(const int32_t* grid_thw, const uint8_t* is_still, int32_t n, int patch,
                                    int tpatch, vitfe_item* items_out, int64_t* total_rows, int64_t* pixel_bytes) {
   if (n < 0 || (n > 0 && (grid_thw == nullptr || items_out == nullptr)) || total_rows == nullptr ||

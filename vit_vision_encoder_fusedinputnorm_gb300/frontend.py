@@ -110,6 +110,19 @@ class FrontEnd:
                      self._stream(stream))
         return cos, sin
 
+    def cu_seqlens(self, b: Batch, max_seqs: int, rows: Optional[int] = None, out=None, info=None, status=None,
+                   stream=None):
+        """(cu_seqlens int32 [max_seqs + 1], seq_info int32 [2] = {sequences, longest})."""
+        torch = self.torch
+        rows = b.live_rows if rows is None else rows
+        if out is None:
+            out = torch.empty(max_seqs + 1, dtype=torch.int32, device=self.device)
+        if info is None:
+            info = torch.empty(2, dtype=torch.int32, device=self.device)
+        B.vitfe_cu_seqlens(self.h, b.items, b.n_items, b.capacity, rows, max_seqs, out, info, status,
+                           self._stream(stream))
+        return out, info
+
     def pos_ids(self, b: Batch, rows: Optional[int] = None, out=None, status=None, stream=None):
         torch = self.torch
         rows = b.live_rows if rows is None else rows
