@@ -260,16 +260,13 @@ def main():
     stream = torch.cuda.Stream(device=dev)
 
     def step(ev=None):
+        # the whole hot path in one launch: embeddings and the RoPE rows of the same items
         if ev is not None:
             ev[0].record(stream)
-        B.vitfe_embed(fe.h, batch.pixels, batch.pixel_bytes, batch.items, batch.n_items, batch.capacity, rows,
-                      out, st, stream)
+        B.vitfe_embed_rope(fe.h, batch.pixels, batch.pixel_bytes, batch.items, batch.n_items, batch.capacity,
+                           rows, out, wl.head_dim, wl.theta, cos, sin, st, stream)
         if ev is not None:
             ev[1].record(stream)
-        B.vitfe_rope(fe.h, batch.items, batch.n_items, batch.capacity, rows, wl.head_dim, wl.theta, cos, sin,
-                     None, stream)
-        if ev is not None:
-            ev[2].record(stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -278,7 +275,7 @@ def main():
     if st.cpu().tolist() != [0, -1]:
         raise RuntimeError(f"device status {st.cpu().tolist()}")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -302,7 +299,6 @@ def main():
         total_ms = float(tt.item())
     ms_step = total_ms / args.steps
     embed_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    rope_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     value = world * rows / (ms_step / 1e3)
 
     # end to end through the C ABI from pinned host buffers: H2D pixels + items, the step,
@@ -343,21 +339,35 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
 
+    def timed(fn, n=8, skip=3):
+        ts = []
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                a0 = torch.cuda.Event(enable_timing=True)
+                a1 = torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                fn()
+                a1.record(stream)
+                a1.synchronize()
+                if i >= skip:
+                    ts.append(a0.elapsed_time(a1))
+        return statistics.median(ts)
+
+    # the two calls the fused launch replaces, and the RoPE expansion alone (HBM-write bound)
+    def unfused():
+        B.vitfe_embed(fe.h, batch.pixels, batch.pixel_bytes, batch.items, batch.n_items, batch.capacity, rows,
+                      out, st, stream)
+        B.vitfe_rope(fe.h, batch.items, batch.n_items, batch.capacity, rows, wl.head_dim, wl.theta, cos, sin,
+                     None, stream)
+
+    unfused_ms = timed(unfused)
+    rope_ms = timed(lambda: B.vitfe_rope(fe.h, batch.items, batch.n_items, batch.capacity, rows, wl.head_dim,
+                                         wl.theta, cos, sin, None, stream))
+
     # standalone normalise + patchify (HBM-bound side path), timed alone
     flat = torch.empty((rows, K), dtype=torch.bfloat16, device=dev)
-    np_ms = []
-    with torch.cuda.stream(stream):
-        for i in range(8):
-            a0 = torch.cuda.Event(enable_timing=True)
-            a1 = torch.cuda.Event(enable_timing=True)
-            a0.record(stream)
-            B.vitfe_normalize_patchify(fe.h, batch.pixels, batch.pixel_bytes, batch.items, batch.n_items,
-                                       batch.capacity, rows, flat, None, stream)
-            a1.record(stream)
-            a1.synchronize()
-            if i >= 3:
-                np_ms.append(a0.elapsed_time(a1))
-    np_ms = statistics.median(np_ms)
+    np_ms = timed(lambda: B.vitfe_normalize_patchify(fe.h, batch.pixels, batch.pixel_bytes, batch.items,
+                                                     batch.n_items, batch.capacity, rows, flat, None, stream))
     np_bytes = batch.pixel_bytes + rows * K * 2
     del flat
 
@@ -371,7 +381,7 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "64 x 1344x1344 uint8 stills, patch 14, tpatch 2, merge 2, K 1176, N 1280, "
                                "RoPE head_dim 80", "rows_per_step": rows,
-                   "step": "vitfe_embed + vitfe_rope (C ABI, device-resident inputs)",
+                   "step": "vitfe_embed_rope: embeddings + RoPE rows in one launch (C ABI, device-resident inputs)",
                    "l2": "inputs (347 MB) and outputs (1.5 GB) exceed L2; no flush",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -380,7 +390,8 @@ def main():
                      "frac_of_sustained": achieved / float(pk.get("bf16_tflops_sustained", peak)),
                      "kernel": "embed_kernel<14>", "flops_per_launch": flops,
                      "kernel_ms": embed_ms},
-        "side_paths": {"rope_ms": rope_ms,
+        "side_paths": {"unfused_embed_then_rope_ms": unfused_ms,
+                       "rope_ms": rope_ms,
                        "rope_gbs": rows * wl.head_dim // 2 * 4 * 2 / (rope_ms / 1e3) / 1e9,
                        "rope_frac_hbm": rows * wl.head_dim // 2 * 4 * 2 / (rope_ms / 1e3) / 1e9 / float(pk["hbm_gbs"]),
                        "normalize_patchify_ms": np_ms,
@@ -388,9 +399,9 @@ def main():
                        "normalize_patchify_frac_hbm": np_bytes / (np_ms / 1e3) / 1e9 / float(pk["hbm_gbs"])},
         "e2e": {"value": world * rows / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        # per step: embed_kernel + rope_expand_kernel (the position table stays cached
-        # in the handle after the warm-up steps built it)
-        "gpu_launches": 2 * args.steps,
+        # per step: one embed_kernel launch that also writes the RoPE rows (the position
+        # table stays cached in the handle after the first warm-up step built it)
+        "gpu_launches": 1 * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

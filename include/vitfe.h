@@ -121,6 +121,18 @@ vitfe_status vitfe_rope(vitfe_t h, const vitfe_item* items, const int32_t* n_ite
                         int32_t max_items, int64_t rows, int head_dim, float theta,
                         float* cos, float* sin, int32_t* status, cudaStream_t stream);
 
+/* vitfe_embed and vitfe_rope over the same items in one launch: the embed
+ * kernel's epilogue warps write each tile's cos/sin rows while the tile's first
+ * accumulator is computed.  Arguments, outputs, pad rows and errors are those of
+ * the two calls, with one status word; items with h or w > VITFE_ROPE_MAX_SIDE
+ * are rejected on the device for both outputs.  The first call with a
+ * (head_dim, theta) pair also launches the table build (see vitfe_rope). */
+vitfe_status vitfe_embed_rope(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes,
+                              const vitfe_item* items, const int32_t* n_items,
+                              int32_t max_items, int64_t rows, void* out, int head_dim,
+                              float theta, float* cos, float* sin, int32_t* status,
+                              cudaStream_t stream);
+
 /* Standalone FusedInputNorm + patchify: writes flatten_patches, bf16
  * [rows][K] in the canonical (C, T, P, P) feature order of §3.2 (the order
  * the Conv3d weight is flattened in).  Same inputs as vitfe_embed. */

@@ -403,3 +403,74 @@ def test_cu_seqlens_bucket_clipping_and_overflow():
     assert cu.cpu().numpy().tolist() == cu_ref[:4].tolist()
     assert int(info[0]) == 3 and st.cpu().tolist() == [5, -1]
     fe.close()
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_embed_rope_one_launch_equals_the_two_calls(name):
+    # the fused launch writes exactly what vitfe_embed and vitfe_rope write, pad rows included
+    P, N, grids = SMALL[name]
+    hd = 80 if P == 14 else 72
+    wl = synth.small_workload(29, grids, patch=P, hidden=N, head_dim=hd, pixels="uniform")
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    rows = b.live_rows + 300
+    st = fe.status_tensor()
+    out, cos, sin = fe.embed_rope(b, hd, wl.theta, rows=rows, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, -1]
+    e = fe.embed(b, rows=rows)
+    c2, s2 = fe.rope(b, hd, wl.theta, rows=rows)
+    torch.cuda.synchronize()
+    assert np.array_equal(U.tensor_bits(out), U.tensor_bits(e))
+    assert np.array_equal(cos.cpu().numpy(), c2.cpu().numpy())
+    assert np.array_equal(sin.cpu().numpy(), s2.cpu().numpy())
+    rc, rs = oracle.rope_workload(wl, bucket_rows=rows)
+    assert np.max(np.abs(cos.cpu().numpy() - rc)) <= U.ROPE_MAX_ABS
+    assert np.max(np.abs(sin.cpu().numpy() - rs)) <= U.ROPE_MAX_ABS
+    ref = oracle.embed_workload(wl, bucket_rows=rows)
+    rel, mx = U.embed_errors(U.bits_to_f64(U.tensor_bits(out)), ref, U.item_starts(wl.items))
+    assert rel <= U.EMBED_REL_FROB and mx <= U.EMBED_MAX_ABS, (rel, mx)
+    fe.close()
+
+
+def test_embed_rope_graph_replay_with_new_items():
+    # one captured fused launch serves buckets whose items change between replays
+    wl = synth.small_workload(31, [(1, 4, 6, 1), (2, 2, 4, 4), (1, 8, 8, 1)], patch=14, hidden=256, head_dim=80)
+    wl2 = synth.small_workload(32, [(1, 6, 6, 1), (1, 2, 10, 1)], patch=14, hidden=256, head_dim=80)
+    fe = _fe(wl)
+    from vit_vision_encoder_fusedinputnorm_gb300 import binding as B
+    R = 256
+    b1 = fe.upload(wl.items, capacity=8)
+    px = torch.zeros(max(b1.pixel_bytes, 1 << 20), dtype=torch.uint8, device="cuda")
+    items = torch.zeros(8 * 24, dtype=torch.uint8, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty((R, 256), dtype=torch.bfloat16, device="cuda")
+    cos = torch.empty((R, 40), dtype=torch.float32, device="cuda")
+    sin = torch.empty_like(cos)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):      # warm: builds the table outside the capture
+        B.vitfe_embed_rope(fe.h, px, px.numel(), items, n, 8, R, out, 80, wl.theta, cos, sin, None, s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        B.vitfe_embed_rope(fe.h, px, px.numel(), items, n, 8, R, out, 80, wl.theta, cos, sin, None, s)
+    for w in (wl, wl2):
+        recs, buf, live = B.pack_items(w.items, w.patch, w.tpatch)
+        px[:buf.size].copy_(torch.from_numpy(buf))
+        arr = np.zeros(8, B.ITEM_DTYPE)
+        arr[:len(recs)] = recs
+        items.copy_(torch.from_numpy(arr.view(np.uint8)))
+        n.fill_(len(recs))
+        out.fill_(3.0)
+        cos.fill_(5.0)
+        g.replay()
+        torch.cuda.synchronize()
+        eb = fe.upload(w.items)
+        e = fe.embed(eb)
+        c2, _ = fe.rope(eb, 80, w.theta)
+        torch.cuda.synchronize()
+        assert np.array_equal(U.tensor_bits(out)[:live], U.tensor_bits(e))
+        assert np.all(U.tensor_bits(out)[live:] == 0)
+        assert np.array_equal(cos.cpu().numpy()[:live], c2.cpu().numpy())
+        assert np.all(cos.cpu().numpy()[live:] == 1.0) and np.all(sin.cpu().numpy()[live:] == 0.0)
+    fe.close()

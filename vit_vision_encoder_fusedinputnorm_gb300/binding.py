@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "VITFE_OK", 1: "VITFE_EINVAL", 2: "VITFE_ENOMEM", 3: "VITFE_E
                 7: "VITFE_EUNSUPPORTED"}
 
 # exported symbols of include/vitfe.h
-EXPORTS = ["vitfe_create", "vitfe_destroy", "vitfe_embed", "vitfe_rope", "vitfe_normalize_patchify",
+EXPORTS = ["vitfe_create", "vitfe_destroy", "vitfe_embed", "vitfe_embed_rope", "vitfe_rope", "vitfe_normalize_patchify",
            "vitfe_pos_ids", "vitfe_cu_seqlens", "vitfe_rope_noalloc", "vitfe_items_from_grid",
            "vitfe_feature_dim", "vitfe_status_str"]
 
@@ -63,6 +63,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.vitfe_destroy.restype = None
     lib.vitfe_embed.argtypes = [P, P, I64, P, P, I32, I64, P, P, P]
     lib.vitfe_embed.restype = ctypes.c_int
+    lib.vitfe_embed_rope.argtypes = [P, P, I64, P, P, I32, I64, P, ctypes.c_int, F32, P, P, P, P]
+    lib.vitfe_embed_rope.restype = ctypes.c_int
     lib.vitfe_rope.argtypes = [P, P, P, I32, I64, ctypes.c_int, F32, P, P, P, P]
     lib.vitfe_rope.restype = ctypes.c_int
     lib.vitfe_rope_noalloc.argtypes = [ctypes.c_int, ctypes.c_int, P, P, I32, I64, ctypes.c_int, F32, P, P, P, P]
@@ -129,6 +131,14 @@ def vitfe_embed(h, pixels, pixel_bytes, items, n_items, max_items, rows, out, st
     _check("vitfe_embed", load().vitfe_embed(h, _ptr(pixels), int(pixel_bytes), _ptr(items), _ptr(n_items),
                                              int(max_items), int(rows), _ptr(out), _ptr(status),
                                              _stream(stream)))
+
+
+def vitfe_embed_rope(h, pixels, pixel_bytes, items, n_items, max_items, rows, out, head_dim, theta, cos, sin,
+                     status=None, stream=None) -> None:
+    _check("vitfe_embed_rope",
+           load().vitfe_embed_rope(h, _ptr(pixels), int(pixel_bytes), _ptr(items), _ptr(n_items), int(max_items),
+                                   int(rows), _ptr(out), int(head_dim), float(theta), _ptr(cos), _ptr(sin),
+                                   _ptr(status), _stream(stream)))
 
 
 def vitfe_rope(h, items, n_items, max_items, rows, head_dim, theta, cos, sin, status=None, stream=None) -> None:

@@ -665,8 +665,7 @@ cudaError_t launch_cu_seqlens(const Ctx& c, const vitfe_item* items, const int32
   return cudaGetLastError();
 }
 
-cudaError_t launch_rope(Ctx& c, const vitfe_item* items, const int32_t* n_items, int max_items, int64_t rows,
-                        int head_dim, float theta, float* cos, float* sin, int32_t* status, cudaStream_t s) {
+cudaError_t rope_table_for(Ctx& c, int head_dim, float theta, cudaStream_t s, const float** tab_out) {
   const int nf = head_dim / 4;
   const size_t slot_floats = (size_t)2 * VITFE_ROPE_MAX_SIDE * (VITFE_ROPE_MAX_HEAD_DIM / 4);
   // the cos/sin table of this (head_dim, theta): built once over every position, then reused
@@ -691,6 +690,16 @@ cudaError_t launch_rope(Ctx& c, const vitfe_item* items, const int32_t* n_items,
     if (e != cudaSuccess) return e;
     if (!transient && cap == cudaStreamCaptureStatusNone) c.rope_built[slot] = true;
   }
+  *tab_out = tab;
+  return cudaSuccess;
+}
+
+cudaError_t launch_rope(Ctx& c, const vitfe_item* items, const int32_t* n_items, int max_items, int64_t rows,
+                        int head_dim, float theta, float* cos, float* sin, int32_t* status, cudaStream_t s) {
+  const int nf = head_dim / 4;
+  const float* tab = nullptr;
+  cudaError_t e = rope_table_for(c, head_dim, theta, s, &tab);
+  if (e != cudaSuccess) return e;
   const int grid = grid_for(rows, kAuxThreads, c.sm_count * 16);   // 8 warps x 32 rows per CTA
   rope_expand_kernel<<<grid, kAuxThreads, 0, s>>>(items, n_items, max_items, c.T, c.M, (int)rows, nf, tab, cos, sin,
                                                   status);

@@ -64,6 +64,11 @@ struct EmbedArgs {
   int tmem_cols;
   int num_tiles;   // 256-row pair tiles
   uint64_t limit_ns;
+  // 2D-RoPE rows written by the same launch (null: embeddings only)
+  const float* rope_tab;   // the handle's axis table: cos [p * nf + i], sin after VITFE_ROPE_MAX_SIDE rows
+  float* rope_cos;
+  float* rope_sin;
+  int rope_nf;             // head_dim / 4
 };
 
 // Shared-memory header (placed before the 1024-aligned tile area).
@@ -274,6 +279,67 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
   return true;
 }
 
+// 2D-RoPE rows ("vLLM 多模态推理｜ViT 性能优化" §3.3 step 3) of 32 consecutive rows
+// [wbase, wbase + 32), one per lane (hp, wp: the lane's row position, -1 for pad rows and
+// rows of invalid items): cos[r] = [tab_cos[hp][0..nf) || tab_cos[wp][0..nf)], sin
+// likewise, pad rows (1, 0).  The warp writes the rows' contiguous range with float4
+// stores; every lane of the warp calls it.
+__device__ __forceinline__ void rope_rows(const EmbedArgs& a, int wbase, int hp, int wp, int lane) {
+  constexpr int kBatch = 4;          // float4 groups per lane whose table loads are in flight together
+  const int nf = a.rope_nf;
+  const int width = 2 * nf;          // floats per row
+  const int nvec = width >> 2;       // float4 per row (head_dim % 8 == 0)
+  const int cnt = min(32, a.rows - wbase);
+  if (cnt <= 0) return;
+  const int total = cnt * nvec;
+  const float* __restrict__ tc = a.rope_tab;
+  const float* __restrict__ ts = a.rope_tab + (size_t)VITFE_ROPE_MAX_SIDE * nf;
+  const bool vec_tab = (nf % 4) == 0;
+  float4* cdst = reinterpret_cast<float4*>(a.rope_cos + (size_t)wbase * width);
+  float4* sdst = reinterpret_cast<float4*>(a.rope_sin + (size_t)wbase * width);
+  for (int f0 = 0; f0 < total; f0 += 32 * kBatch) {
+    float4 cv[kBatch], sv[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int f = f0 + 32 * k + lane;
+      const int rr = min(f / nvec, 31);
+      const int h = __shfl_sync(0xffffffffu, hp, rr);
+      const int w = __shfl_sync(0xffffffffu, wp, rr);
+      cv[k] = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+      sv[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (f < total && h >= 0) {
+        const int col = 4 * (f - rr * nvec);
+        if (vec_tab) {
+          const int p = col < nf ? h : w;
+          const int i = col < nf ? col : col - nf;
+          cv[k] = __ldg(reinterpret_cast<const float4*>(tc + (size_t)p * nf + i));
+          sv[k] = __ldg(reinterpret_cast<const float4*>(ts + (size_t)p * nf + i));
+        } else {
+          float c4[4], s4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int cc = col + e;
+            const int p = cc < nf ? h : w;
+            const int i = cc < nf ? cc : cc - nf;
+            c4[e] = __ldg(tc + (size_t)p * nf + i);
+            s4[e] = __ldg(ts + (size_t)p * nf + i);
+          }
+          cv[k] = make_float4(c4[0], c4[1], c4[2], c4[3]);
+          sv[k] = make_float4(s4[0], s4[1], s4[2], s4[3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int f = f0 + 32 * k + lane;
+      if (f < total) {
+        __stcs(cdst + f, cv[k]);
+        __stcs(sdst + f, sv[k]);
+      }
+    }
+  }
+}
+
 // 32 contiguous bytes (16 bf16) with one 256-bit store, evict-first.
 __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
   asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
@@ -368,7 +434,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     ItemTab tab{hs->start, hs->bad, hs->still, &hs->tab};
     build_item_table(args.items, args.n_items, args.max_items, args.pixel_bytes, P, args.T, args.M,
-                     args.rows, 0x7fffffff, tab);
+                     args.rows, args.rope_cos != nullptr ? VITFE_ROPE_MAX_SIDE : 0x7fffffff, tab);
   }
   if (warp == kMmaWarp) {
     tmem_alloc_pair(smem_u32(&hs->tmem_base), (uint32_t)args.tmem_cols);
@@ -592,21 +658,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int r = r0 + rloc;
       const bool in_bucket = r < args.rows;
       bool valid = false;
+      int hp = -1, wp = -1;
       if (r < hs->tab.live) {
         const int i = find_item(hs->start, hs->tab.n, r);
         valid = !tab_bit(hs->bad, i);
+        if (valid && args.rope_cos != nullptr) {
+          const vitfe_item it = args.items[i];
+          int tg;
+          decode_local(r - hs->start[i], it.h, it.w, args.M, tg, hp, wp);
+        }
       }
+      const int rope_wbase = r0 + (int)rank * kTileM + q * 32;
       __nv_bfloat16* orow = args.out + (size_t)r * (size_t)args.N;
       if (kind == kPad) {
         if (in_bucket) {
           const uint4 z = make_uint4(0u, 0u, 0u, 0u);
           for (int c = 0; c < args.N; c += 8) *reinterpret_cast<uint4*>(orow + c) = z;
         }
+        if (args.rope_cos != nullptr) rope_rows(args, rope_wbase, hp, wp, lane);
         continue;
       }
+      // the RoPE rows of this warp's 32 tile rows go out after the second pass's accumulator:
+      // the producers are idle then (they fill the next tile's A during the first and last
+      // passes) and the epilogue waits for the next accumulator anyway
+      const int rope_pass = args.npass > 1 ? 1 : 0;
       for (int p = 0; p < args.npass; ++p) {
         const uint32_t buf = na & 1u;
-        if (!mbar_wait_cl(smem_u32(&hs->acc_full[buf]), (na >> 1) & 1u, abort_flag, args.limit_ns, 64)) {
+        // warp-uniform wait: tcgen05.ld below (and the RoPE rows' shuffles) need the whole warp
+        if (!mbar_wait_warp<true>(smem_u32(&hs->acc_full[buf]), (na >> 1) & 1u, abort_flag, args.limit_ns, 64)) {
           ok = false;
           break;
         }
@@ -644,6 +723,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive_cluster(acc_empty_L + 8u * buf);
         ++na;
+        if (args.rope_cos != nullptr && p == rope_pass) rope_rows(args, rope_wbase, hp, wp, lane);
       }
     }
   }
@@ -714,7 +794,8 @@ cudaError_t embed_configure(Ctx& c) {
 
 cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_bytes,
                          const vitfe_item* items, const int32_t* n_items, int max_items,
-                         int64_t rows, void* out, int32_t* status, cudaStream_t s) {
+                         int64_t rows, void* out, int32_t* status, cudaStream_t s, const float* rope_tab,
+                         int rope_nf, float* rope_cos, float* rope_sin) {
   EmbedArgs a;
   a.pixels = pixels;
   a.pixel_bytes = pixel_bytes;
@@ -737,6 +818,10 @@ cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_byte
   while (a.tmem_cols < 2 * c.bn) a.tmem_cols <<= 1;
   a.num_tiles = (int)((rows + kPairRows - 1) / kPairRows);
   a.limit_ns = c.wait_limit_ns;
+  a.rope_tab = rope_tab;
+  a.rope_cos = rope_cos;
+  a.rope_sin = rope_sin;
+  a.rope_nf = rope_nf;
   int pairs = a.num_tiles < c.max_clusters ? a.num_tiles : c.max_clusters;
   if (pairs < 1) pairs = 1;
   const int grid = 2 * pairs;

@@ -182,6 +182,26 @@ vitfe_status vitfe_embed(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes, 
                                        stream));
 }
 
+vitfe_status vitfe_embed_rope(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes, const vitfe_item* items,
+                              const int32_t* n_items, int32_t max_items, int64_t rows, void* out, int head_dim,
+                              float theta, float* cos, float* sin, int32_t* status, cudaStream_t stream) {
+  vitfe_status st = check_common(h, items, n_items, max_items, rows);
+  if (st != VITFE_OK) return st;
+  if (pixels == nullptr || pixel_bytes < 0 || !aligned(pixels, 16)) return VITFE_EINVAL;
+  if ((out == nullptr && rows > 0) || !aligned(out, 16)) return VITFE_EINVAL;
+  if (head_dim < 8 || head_dim > VITFE_ROPE_MAX_HEAD_DIM || (head_dim % 8) != 0) return VITFE_EINVAL;
+  if (!std::isfinite(theta) || !(theta > 0.0f)) return VITFE_EINVAL;
+  if (rows > 0 && (cos == nullptr || sin == nullptr)) return VITFE_EINVAL;
+  if (!aligned(cos, 16) || !aligned(sin, 16)) return VITFE_EINVAL;
+  if (status && !aligned(status, 4)) return VITFE_EINVAL;
+  if (!h->c.embed_ok) return VITFE_EUNSUPPORTED;
+  const float* tab = nullptr;
+  cudaError_t e = vitfe::rope_table_for(h->c, head_dim, theta, stream, &tab);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(vitfe::launch_embed(h->c, pixels, pixel_bytes, items, n_items, max_items, rows, out, status,
+                                       stream, tab, head_dim / 4, cos, sin));
+}
+
 vitfe_status vitfe_rope(vitfe_t h, const vitfe_item* items, const int32_t* n_items, int32_t max_items,
                         int64_t rows, int head_dim, float theta, float* cos, float* sin, int32_t* status,
                         cudaStream_t stream) {

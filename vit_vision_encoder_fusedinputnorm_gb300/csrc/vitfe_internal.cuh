@@ -463,13 +463,16 @@ __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
   if constexpr (kCluster) return mbar_try_wait_cluster(bar, parity);
   else return mbar_try_wait(bar, parity);
 }
+// sleep_ns > 0: after a few failed polls the warp backs off with __nanosleep, leaving its
+// scheduler's issue slots to the warps it shares them with.
 template <bool kCluster>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                               uint64_t limit_ns) {
+                                               uint64_t limit_ns, uint32_t sleep_ns = 0) {
   if (__all_sync(0xffffffffu, mbar_poll<kCluster>(bar, parity))) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (__all_sync(0xffffffffu, mbar_poll<kCluster>(bar, parity))) return true;
+    if (sleep_ns && i > 2) __nanosleep(sleep_ns);
     if ((i & 15u) == 0) {
       const bool stop = *abort_flag != 0 || global_timer_ns() - t0 > limit_ns;
       if (__any_sync(0xffffffffu, stop)) {
@@ -494,10 +497,18 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
 // ---------------------------------------------------------------------------
 // launchers (defined in the kernel translation units)
 // ---------------------------------------------------------------------------
+// rope_cos != nullptr: the same launch also writes the 2D-RoPE rows from rope_tab
+// (an axis table from rope_table_for; nf = head_dim / 4).
 cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_bytes,
                          const vitfe_item* items, const int32_t* n_items, int max_items,
-                         int64_t rows, void* out, int32_t* status, cudaStream_t s);
+                         int64_t rows, void* out, int32_t* status, cudaStream_t s,
+                         const float* rope_tab = nullptr, int rope_nf = 0, float* rope_cos = nullptr,
+                         float* rope_sin = nullptr);
 cudaError_t embed_configure(Ctx& c);
+// The handle's cos/sin axis table of (head_dim, theta): found in its slots, or built there
+// (one launch on `s`) the first time.  Layout: cos at [p * nf + i], sin at
+// [VITFE_ROPE_MAX_SIDE * nf + p * nf + i], nf = head_dim / 4, p < VITFE_ROPE_MAX_SIDE.
+cudaError_t rope_table_for(Ctx& c, int head_dim, float theta, cudaStream_t s, const float** tab_out);
 cudaError_t launch_rope(Ctx& c, const vitfe_item* items, const int32_t* n_items,
                         int max_items, int64_t rows, int head_dim, float theta, float* cos,
                         float* sin, int32_t* status, cudaStream_t s);

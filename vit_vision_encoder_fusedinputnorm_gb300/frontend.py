@@ -98,6 +98,21 @@ class FrontEnd:
                                    status, self._stream(stream))
         return out
 
+    def embed_rope(self, b: Batch, head_dim: int, theta: float, rows: Optional[int] = None, out=None, cos=None,
+                   sin=None, status=None, stream=None):
+        """embed + rope in one launch: (out, cos, sin)."""
+        torch = self.torch
+        rows = b.live_rows if rows is None else rows
+        if out is None:
+            out = torch.empty((rows, self.hidden), dtype=torch.bfloat16, device=self.device)
+        if cos is None:
+            cos = torch.empty((rows, head_dim // 2), dtype=torch.float32, device=self.device)
+        if sin is None:
+            sin = torch.empty((rows, head_dim // 2), dtype=torch.float32, device=self.device)
+        B.vitfe_embed_rope(self.h, b.pixels, b.pixel_bytes, b.items, b.n_items, b.capacity, rows, out, head_dim,
+                           theta, cos, sin, status, self._stream(stream))
+        return out, cos, sin
+
     def rope(self, b: Batch, head_dim: int, theta: float, rows: Optional[int] = None, cos=None, sin=None,
              status=None, stream=None):
         torch = self.torch
