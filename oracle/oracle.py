@@ -28,6 +28,13 @@ What it computes, step by step, with the passage each step follows:
    each row is [cos(hpos*w_i) ... || cos(wpos*w_i) ...], likewise for sin.
    Same page, §3.3 steps 1, 3 and 5.
 
+6. Attention sequence boundaries: one sequence per temporal group of each item,
+   h*w tokens long, in item order.  Same page, §3.4 (cu_seqlens) read with
+   §3.3 (the encoder models single images and frames).
+7. RoPE applied to Q/K in each vision block (same page, §3.3 step 6), in the
+   rotate-half form: feature i of a head and feature i + head_dim/2 rotate as
+   one pair by the angle of table column i.
+
 Readings where the pages are silent (each also listed in the design notes):
 the first step's order is rescale, subtract the mean, divide by std; the
 rotary width is head_dim / 2; a padded bucket's rows past the live rows are
@@ -46,7 +53,7 @@ __all__ = [
     "bf16_bits_to_f64", "normalize", "patchify", "normalize_patchify_item",
     "embed_rows", "embed_item", "embed_workload", "pos_ids", "rope_tables",
     "rope_workload", "pos_ids_workload", "normalize_patchify_workload", "cu_seqlens",
-    "cu_seqlens_workload",
+    "cu_seqlens_workload", "rope_apply",
     "patch_coords",
 ]
 
@@ -289,6 +296,28 @@ def rope_tables(pos: np.ndarray, head_dim: int, theta: float) -> Tuple[np.ndarra
     cos[pad] = 1.0
     sin[pad] = 0.0
     return cos, sin
+
+
+def rope_apply(x: np.ndarray, cos: np.ndarray, sin: np.ndarray) -> np.ndarray:
+    """RoPE applied to one projection (Q or K), float64 [rows][heads][head_dim].
+
+    "vLLM 多模态推理｜ViT 性能优化", §3.3 step 6 ("apply RoPE to Q/K in every
+    VisionBlock").  The tables are [rows][head_dim/2] (the [H || W] layout of
+    step 3); the page does not spell the rotation out, and this takes the
+    rotate-half form of a head_dim-wide rotary embedding whose two halves repeat
+    the table: with h = head_dim / 2, c = cos[r][i], s = sin[r][i],
+        y[i]     = x[i] * c - x[i + h] * s
+        y[i + h] = x[i + h] * c + x[i] * s        (i < h)
+    for every head.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    h = x.shape[-1] // 2
+    if cos.shape[-1] != h or sin.shape[-1] != h:
+        raise ValueError("tables must be [rows][head_dim/2]")
+    c = np.asarray(cos, dtype=np.float64)[:, None, :]
+    s = np.asarray(sin, dtype=np.float64)[:, None, :]
+    x1, x2 = x[..., :h], x[..., h:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
 
 
 def rope_workload(wl, items=None, bucket_rows=None, head_dim=None, theta=None):

@@ -303,6 +303,54 @@ def test_pos_ids_agree_with_patch_coords():
     assert np.array_equal(oracle.pos_ids(3, 4, 6, 2), c[:, 1:])
 
 
+# ---------------------------------------------------------------- RoPE applied to Q/K
+
+def _apply_case(seed=0, rows=7, heads=3, hd=16):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((rows, heads, hd))
+    pos = np.stack([rng.integers(0, 50, rows), rng.integers(0, 50, rows)], 1)
+    c, s = oracle.rope_tables(pos, hd, 10000.0)
+    return x, pos, c, s
+
+
+def test_rope_apply_is_complex_rotation_of_half_pairs():
+    # (x_i, x_{i+h}) as the complex number x_i + 1j*x_{i+h}, multiplied by e^{1j*angle}
+    x, pos, c, s = _apply_case()
+    h = x.shape[-1] // 2
+    ang = np.arctan2(s, c)[:, None, :]
+    z = (x[..., :h] + 1j * x[..., h:]) * np.exp(1j * ang)
+    y = oracle.rope_apply(x, c, s)
+    assert np.allclose(y[..., :h], z.real, atol=1e-12) and np.allclose(y[..., h:], z.imag, atol=1e-12)
+
+
+def test_rope_apply_identity_at_origin_norms_and_inverse():
+    x, pos, c, s = _apply_case(1)
+    h = x.shape[-1] // 2
+    zero = np.zeros((len(x), 2), np.int64)
+    c0, s0 = oracle.rope_tables(zero, x.shape[-1], 10000.0)
+    assert np.array_equal(oracle.rope_apply(x, c0, s0), x)
+    y = oracle.rope_apply(x, c, s)
+    assert np.allclose(np.hypot(y[..., :h], y[..., h:]), np.hypot(x[..., :h], x[..., h:]), atol=1e-12)
+    assert np.allclose(oracle.rope_apply(y, c, -s), x, atol=1e-12)
+
+
+def test_rope_apply_scores_depend_on_relative_position_only():
+    # <R(p) q, R(p') k> is unchanged when both positions shift by the same offset (per axis)
+    rng = np.random.default_rng(2)
+    hd = 16
+    q = rng.standard_normal((1, 1, hd))
+    k = rng.standard_normal((1, 1, hd))
+
+    def score(pq, pk):
+        cq, sq = oracle.rope_tables(np.array([pq]), hd, 100.0)
+        ck, sk = oracle.rope_tables(np.array([pk]), hd, 100.0)
+        return float(np.sum(oracle.rope_apply(q, cq, sq) * oracle.rope_apply(k, ck, sk)))
+
+    base = score((3, 5), (1, 9))
+    assert abs(score((13, 25), (11, 29)) - base) < 1e-9
+    assert abs(score((3, 5), (2, 9)) - base) > 1e-6      # and does change with the offset
+
+
 # ---------------------------------------------------------------- cu_seqlens
 
 def test_cu_seqlens_boundaries_are_where_item_or_frame_group_changes():
