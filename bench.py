@@ -369,6 +369,15 @@ def main():
     np_ms = timed(lambda: B.vitfe_normalize_patchify(fe.h, batch.pixels, batch.pixel_bytes, batch.items,
                                                      batch.n_items, batch.capacity, rows, flat, None, stream))
     np_bytes = batch.pixel_bytes + rows * K * 2
+
+    # RoPE applied to Q and K (16 + 16 heads of 80, views into a packed [rows][Q | K | V]
+    # buffer), from the step's cos/sin tables: HBM bound, in place
+    heads = N // wl.head_dim
+    qkv = torch.zeros((rows, 3 * N), dtype=torch.bfloat16, device=dev)
+    apply_ms = timed(lambda: B.vitfe_rope_apply(cos, sin, rows, wl.head_dim, qkv, heads, 3 * N, qkv[:, N:],
+                                                heads, 3 * N, stream))
+    apply_bytes = rows * (2 * heads * wl.head_dim * 2 * 2 + wl.head_dim // 2 * 4 * 2)
+    del qkv
     del flat
 
     pk, pk_kind = peaks()
@@ -394,6 +403,9 @@ def main():
                        "rope_ms": rope_ms,
                        "rope_gbs": rows * wl.head_dim // 2 * 4 * 2 / (rope_ms / 1e3) / 1e9,
                        "rope_frac_hbm": rows * wl.head_dim // 2 * 4 * 2 / (rope_ms / 1e3) / 1e9 / float(pk["hbm_gbs"]),
+                       "rope_apply_qk_ms": apply_ms,
+                       "rope_apply_qk_gbs": apply_bytes / (apply_ms / 1e3) / 1e9,
+                       "rope_apply_qk_frac_hbm": apply_bytes / (apply_ms / 1e3) / 1e9 / float(pk["hbm_gbs"]),
                        "normalize_patchify_ms": np_ms,
                        "normalize_patchify_gbs": np_bytes / (np_ms / 1e3) / 1e9,
                        "normalize_patchify_frac_hbm": np_bytes / (np_ms / 1e3) / 1e9 / float(pk["hbm_gbs"])},

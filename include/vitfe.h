@@ -147,6 +147,21 @@ vitfe_status vitfe_pos_ids(vitfe_t h, const vitfe_item* items, const int32_t* n_
                            int32_t max_items, int64_t rows, int32_t* pos, int32_t* status,
                            cudaStream_t stream);
 
+/* RoPE applied to Q and K ("vLLM 多模态推理｜ViT 性能优化" §3.3 step 6), in place,
+ * in the rotate-half form: for every row r, head and i < head_dim/2,
+ *   y[i]              = x[i] * cos[r][i] - x[i + head_dim/2] * sin[r][i]
+ *   y[i + head_dim/2] = x[i + head_dim/2] * cos[r][i] + x[i] * sin[r][i]
+ * in fp32, rounded to nearest-even bf16.  cos, sin: the [rows][head_dim/2] tables
+ * of vitfe_rope (device fp32, 16-byte aligned).  q: device bf16, row r head h at
+ * q + r * q_row_stride + h * head_dim (elements; stride a multiple of 4, at least
+ * heads_q * head_dim; 8-byte aligned), so Q may be a view into a packed QKV
+ * buffer; k likewise.  heads_q or heads_k may be 0 (that pointer is then
+ * unused).  head_dim % 8 == 0, 8 <= head_dim <= VITFE_ROPE_MAX_HEAD_DIM.
+ * Needs no handle; capturable. */
+vitfe_status vitfe_rope_apply(const float* cos, const float* sin, int64_t rows, int head_dim,
+                              void* q, int32_t heads_q, int64_t q_row_stride, void* k,
+                              int32_t heads_k, int64_t k_row_stride, cudaStream_t stream);
+
 /* Attention sequence boundaries ("vLLM 多模态推理｜ViT 性能优化" §3.4): the
  * encoder's attention keeps images apart, and its variable-length kernels take
  * the first row of every sequence.  Each temporal group of an item (a still: the

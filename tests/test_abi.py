@@ -98,6 +98,21 @@ def test_calls_reject_null_handle(lib):
         assert e.value.code == 1
 
 
+def test_rope_apply_rejects_bad_shapes_before_launching(lib):
+    # host validation only: nothing is launched, so any pointer values work here
+    bad = [(16, 16, 10, 84, 16, 2, 168, 16, 2, 168),      # head_dim not a multiple of 8
+           (16, 16, 10, 80, 16, 2, 100, 16, 2, 160),      # q stride below heads * head_dim
+           (16, 16, 10, 80, 16, 2, 162, 16, 2, 160),      # q stride not a multiple of 4
+           (16, 16, 10, 80, 12, 2, 160, 16, 2, 160),      # q not 8-byte aligned
+           (24, 16, 10, 80, 16, 2, 160, 16, 2, 160),      # cos not 16-byte aligned
+           (16, 16, -1, 80, 16, 2, 160, 16, 2, 160),      # negative rows
+           (16, 16, 10, 80, None, 2, 160, 16, 2, 160)]    # heads but no pointer
+    for args in bad:
+        with pytest.raises(B.VitfeError) as e:
+            B.vitfe_rope_apply(*args)
+        assert e.value.code == 1
+
+
 def test_noalloc_rope_rejects_sizes_beyond_its_static_table(lib):
     # head_dim above 128 does not fit the fixed scratch table: a clear error, nothing launched
     with pytest.raises(B.VitfeError) as e:

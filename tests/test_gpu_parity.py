@@ -474,3 +474,38 @@ def test_embed_rope_graph_replay_with_new_items():
         assert np.array_equal(cos.cpu().numpy()[:live], c2.cpu().numpy())
         assert np.all(cos.cpu().numpy()[live:] == 1.0) and np.all(sin.cpu().numpy()[live:] == 0.0)
     fe.close()
+
+
+@pytest.mark.parametrize("hd,hq,hk", [(80, 16, 16), (72, 3, 5), (64, 2, 0), (8, 0, 3), (16, 1, 1)])
+def test_rope_apply_vs_oracle_in_a_packed_qkv_buffer(hd, hq, hk):
+    # Q and K are views into [rows][Q | K | V]; V and the padding must stay untouched
+    from vit_vision_encoder_fusedinputnorm_gb300 import binding as B
+    rng = np.random.default_rng(hd + hq)
+    rows = 333
+    pos = np.stack([rng.integers(0, 90, rows), rng.integers(0, 90, rows)], 1)
+    pos[-5:] = -1                                       # a few bucket-pad rows (identity)
+    c64, s64 = oracle.rope_tables(pos, hd, 10000.0)
+    c32, s32 = c64.astype(np.float32), s64.astype(np.float32)
+    width = (hq + hk + 2) * hd + 4                      # + V heads and 4 elements of padding
+    x = rng.standard_normal((rows, width)).astype(np.float32)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    before = U.tensor_bits(xb)
+    buf = xb.cuda()
+    cos_d = torch.from_numpy(c32).cuda()
+    sin_d = torch.from_numpy(s32).cuda()
+    q = buf if hq else None
+    k = buf[:, hq * hd:] if hk else None
+    B.vitfe_rope_apply(cos_d, sin_d, rows, hd, q, hq, width, k, hk, width)
+    torch.cuda.synchronize()
+    got = U.tensor_bits(buf)
+    xin = U.bits_to_f64(before)
+    for h0, nh in ((0, hq), (hq, hk)):
+        if nh == 0:
+            continue
+        seg = xin[:, h0 * hd:(h0 + nh) * hd].reshape(rows, nh, hd)
+        ref = oracle.rope_apply(seg, c32.astype(np.float64), s32.astype(np.float64)).reshape(rows, nh * hd)
+        g = got[:, h0 * hd:(h0 + nh) * hd]
+        assert int(U.ulp_distance(g, U.f64_to_bf16_bits(ref)).max()) <= 1
+    # pad rows rotate by the identity: bit-exact; everything past Q and K untouched
+    assert np.array_equal(got[-5:], before[-5:])
+    assert np.array_equal(got[:, (hq + hk) * hd:], before[:, (hq + hk) * hd:])

@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "VITFE_OK", 1: "VITFE_EINVAL", 2: "VITFE_ENOMEM", 3: "VITFE_E
 
 # exported symbols of include/vitfe.h
 EXPORTS = ["vitfe_create", "vitfe_destroy", "vitfe_embed", "vitfe_embed_rope", "vitfe_rope", "vitfe_normalize_patchify",
-           "vitfe_pos_ids", "vitfe_cu_seqlens", "vitfe_rope_noalloc", "vitfe_items_from_grid",
+           "vitfe_pos_ids", "vitfe_cu_seqlens", "vitfe_rope_apply", "vitfe_rope_noalloc",
+           "vitfe_items_from_grid",
            "vitfe_feature_dim", "vitfe_status_str"]
 
 ITEM_DTYPE = np.dtype([("pixel_offset", "<i8"), ("t", "<i4"), ("h", "<i4"), ("w", "<i4"),
@@ -75,6 +76,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.vitfe_pos_ids.restype = ctypes.c_int
     lib.vitfe_cu_seqlens.argtypes = [P, P, P, I32, I64, I32, P, P, P, P]
     lib.vitfe_cu_seqlens.restype = ctypes.c_int
+    lib.vitfe_rope_apply.argtypes = [P, P, I64, ctypes.c_int, P, I32, I64, P, I32, I64, P]
+    lib.vitfe_rope_apply.restype = ctypes.c_int
     lib.vitfe_items_from_grid.argtypes = [P, P, I32, ctypes.c_int, ctypes.c_int, P,
                                           ctypes.POINTER(I64), ctypes.POINTER(I64)]
     lib.vitfe_items_from_grid.restype = ctypes.c_int
@@ -172,6 +175,13 @@ def vitfe_cu_seqlens(h, items, n_items, max_items, rows, max_seqs, cu_seqlens, s
     _check("vitfe_cu_seqlens", load().vitfe_cu_seqlens(h, _ptr(items), _ptr(n_items), int(max_items), int(rows),
                                                        int(max_seqs), _ptr(cu_seqlens), _ptr(seq_info),
                                                        _ptr(status), _stream(stream)))
+
+
+def vitfe_rope_apply(cos, sin, rows, head_dim, q, heads_q, q_row_stride, k, heads_k, k_row_stride,
+                     stream=None) -> None:
+    _check("vitfe_rope_apply", load().vitfe_rope_apply(_ptr(cos), _ptr(sin), int(rows), int(head_dim), _ptr(q),
+                                                       int(heads_q), int(q_row_stride), _ptr(k), int(heads_k),
+                                                       int(k_row_stride), _stream(stream)))
 
 
 def vitfe_items_from_grid(grid_thw: np.ndarray, is_still: Optional[np.ndarray], patch: int,

@@ -49,6 +49,72 @@ __global__ void __launch_bounds__(kAuxThreads) pos_ids_kernel(const vitfe_item* 
 }
 
 // ---------------------------------------------------------------------------
+// RoPE applied to Q/K ("vLLM 多模态推理｜ViT 性能优化" §3.3 step 6), rotate-half form:
+// per head, feature i and feature i + hh (hh = head_dim / 2) rotate as one pair by the
+// angle of table column i:  y[i] = x[i] c - x[i+hh] s,  y[i+hh] = x[i+hh] c + x[i] s,
+// c = cos[r][i], s = sin[r][i]; fp32 arithmetic, bf16 round-to-nearest-even, in place.
+// One warp per row at a time; lane units are (head, group of 4 pairs) of the row, Q heads
+// first, walked 32 at a time without division.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void bf16x4_to_f32(uint2 v, float* f) {
+  f[0] = __uint_as_float(v.x << 16);
+  f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(v.y << 16);
+  f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+}
+__device__ __forceinline__ uint2 f32_to_bf16x4(const float* f) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]);
+  __nv_bfloat162 b = __floats2bfloat162_rn(f[2], f[3]);
+  return make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+}
+
+__global__ void __launch_bounds__(kAuxThreads) rope_apply_kernel(const float* __restrict__ cos,
+                                                                 const float* __restrict__ sin, int rows, int hh,
+                                                                 int heads_q, int heads_k, __nv_bfloat16* q,
+                                                                 long long q_stride, __nv_bfloat16* k,
+                                                                 long long k_stride) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
+  const int nw = (int)((gridDim.x * (unsigned)blockDim.x) >> 5);
+  const int G = hh >> 2;                       // groups of 4 pairs per head
+  const int units = (heads_q + heads_k) * G;   // per row
+  const int h0 = lane / G, j0 = lane - h0 * G;
+  const int dh = 32 / G, dj = 32 - dh * G;     // a step of 32 units in (head, group)
+  for (int r = gw; r < rows; r += nw) {
+    const float* cr = cos + (size_t)r * hh;
+    const float* sr = sin + (size_t)r * hh;
+    int hd = h0, j = j0;
+#pragma unroll 2
+    for (int u = lane; u < units; u += 32) {
+      __nv_bfloat16* x = (hd < heads_q) ? q + (size_t)r * q_stride + (size_t)hd * (2 * hh)
+                                        : k + (size_t)r * k_stride + (size_t)(hd - heads_q) * (2 * hh);
+      uint2* p1 = reinterpret_cast<uint2*>(x + 4 * j);
+      uint2* p2 = reinterpret_cast<uint2*>(x + hh + 4 * j);
+      const float4 c4 = __ldg(reinterpret_cast<const float4*>(cr + 4 * j));
+      const float4 s4 = __ldg(reinterpret_cast<const float4*>(sr + 4 * j));
+      float a[4], b[4], ya[4], yb[4];
+      bf16x4_to_f32(*p1, a);
+      bf16x4_to_f32(*p2, b);
+      const float c[4] = {c4.x, c4.y, c4.z, c4.w};
+      const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        ya[e] = fmaf(a[e], c[e], -(b[e] * sn[e]));
+        yb[e] = fmaf(b[e], c[e], a[e] * sn[e]);
+      }
+      *p1 = f32_to_bf16x4(ya);
+      *p2 = f32_to_bf16x4(yb);
+      hd += dh;
+      j += dj;
+      if (j >= G) {
+        j -= G;
+        ++hd;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Attention sequence boundaries ("vLLM 多模态推理｜ViT 性能优化" §3.4): the encoder's
 // attention keeps each image apart, so its varlen kernels take the first row of every
 // sequence.  The encoder sees single images and single frames (§3.3), so each temporal
@@ -654,6 +720,22 @@ cudaError_t launch_pos_ids(const Ctx& c, const vitfe_item* items, const int32_t*
   const int grid = grid_for(rows, kAuxThreads, c.sm_count * 8);
   pos_ids_kernel<<<grid, kAuxThreads, 0, s>>>(items, n_items, max_items, c.T, c.M, (int)rows,
                                                reinterpret_cast<int2*>(pos), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_apply(const float* cos, const float* sin, int64_t rows, int head_dim, void* q,
+                              int heads_q, int64_t q_stride, void* k, int heads_k, int64_t k_stride,
+                              cudaStream_t s) {
+  if (rows == 0 || heads_q + heads_k == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int warps_per_cta = kAuxThreads / 32;
+  const int grid = grid_for(rows, warps_per_cta, sms * 8);
+  rope_apply_kernel<<<grid, kAuxThreads, 0, s>>>(cos, sin, (int)rows, head_dim / 2, heads_q, heads_k,
+                                                 static_cast<__nv_bfloat16*>(q), q_stride,
+                                                 static_cast<__nv_bfloat16*>(k), k_stride);
   return cudaGetLastError();
 }
 

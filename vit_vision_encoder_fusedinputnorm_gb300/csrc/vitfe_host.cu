@@ -250,6 +250,26 @@ vitfe_status vitfe_cu_seqlens(vitfe_t h, const vitfe_item* items, const int32_t*
                                             status, stream));
 }
 
+vitfe_status vitfe_rope_apply(const float* cos, const float* sin, int64_t rows, int head_dim, void* q,
+                              int32_t heads_q, int64_t q_row_stride, void* k, int32_t heads_k,
+                              int64_t k_row_stride, cudaStream_t stream) {
+  if (rows < 0 || rows > kMaxRows) return VITFE_EINVAL;
+  if (head_dim < 8 || head_dim > VITFE_ROPE_MAX_HEAD_DIM || (head_dim % 8) != 0) return VITFE_EINVAL;
+  if (heads_q < 0 || heads_k < 0 || heads_q > 4096 || heads_k > 4096) return VITFE_EINVAL;
+  if (rows > 0 && (cos == nullptr || sin == nullptr)) return VITFE_EINVAL;
+  if (!aligned(cos, 16) || !aligned(sin, 16)) return VITFE_EINVAL;
+  if (heads_q > 0) {
+    if (q == nullptr || !aligned(q, 8) || q_row_stride < (int64_t)heads_q * head_dim || (q_row_stride % 4) != 0)
+      return VITFE_EINVAL;
+  }
+  if (heads_k > 0) {
+    if (k == nullptr || !aligned(k, 8) || k_row_stride < (int64_t)heads_k * head_dim || (k_row_stride % 4) != 0)
+      return VITFE_EINVAL;
+  }
+  return from_cuda(vitfe::launch_rope_apply(cos, sin, rows, head_dim, q, heads_q, q_row_stride, k, heads_k,
+                                            k_row_stride, stream));
+}
+
 vitfe_status vitfe_items_from_grid(const int32_t* grid_thw, const uint8_t* is_still, int32_t n, int patch,
                                    int tpatch, vitfe_item* items_out, int64_t* total_rows, int64_t* pixel_bytes) {
   if (n < 0 || (n > 0 && (grid_thw == nullptr || items_out == nullptr)) || total_rows == nullptr ||

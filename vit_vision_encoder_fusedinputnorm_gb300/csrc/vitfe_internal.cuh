@@ -516,6 +516,9 @@ cudaError_t launch_normalize_patchify(const Ctx& c, const uint8_t* pixels, int64
                                       const vitfe_item* items, const int32_t* n_items,
                                       int max_items, int64_t rows, void* out, int32_t* status,
                                       cudaStream_t s);
+cudaError_t launch_rope_apply(const float* cos, const float* sin, int64_t rows, int head_dim, void* q,
+                              int heads_q, int64_t q_stride, void* k, int heads_k, int64_t k_stride,
+                              cudaStream_t s);
 cudaError_t launch_cu_seqlens(const Ctx& c, const vitfe_item* items, const int32_t* n_items, int max_items,
                               int64_t rows, int max_seqs, int32_t* cu, int32_t* info, int32_t* status,
                               cudaStream_t s);
