@@ -34,6 +34,9 @@ What it computes, step by step, with the passage each step follows:
 7. RoPE applied to Q/K in each vision block (same page, §3.3 step 6), in the
    rotate-half form: feature i of a head and feature i + head_dim/2 rotate as
    one pair by the angle of table column i.
+8. A folded-still variant of step 3 (not part of the method; reported on its
+   own): a still's equal temporal slices of A multiply the summed weight
+   slices rounded once to bf16.
 
 Readings where the pages are silent (each also listed in the design notes):
 the first step's order is rescale, subtract the mean, divide by std; the
@@ -53,7 +56,8 @@ __all__ = [
     "bf16_bits_to_f64", "normalize", "patchify", "normalize_patchify_item",
     "embed_rows", "embed_item", "embed_workload", "pos_ids", "rope_tables",
     "rope_workload", "pos_ids_workload", "normalize_patchify_workload", "cu_seqlens",
-    "cu_seqlens_workload", "rope_apply",
+    "cu_seqlens_workload", "rope_apply", "round_to_bf16_bits", "fold_still_weight", "embed_folded_item",
+    "embed_folded_workload",
     "patch_coords",
 ]
 
@@ -197,6 +201,65 @@ def embed_workload(wl, items: Optional[Sequence[int]] = None, bucket_rows: Optio
             continue
         out[sel] = embed_item(it.pixels, it.t, it.h, it.w, wl.W_bits, wl.b_bits,
                               rows=sample[sel] - starts[j], **common)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# 3c. folded-still variant (an approximation of step 3, reported on its own)
+# ---------------------------------------------------------------------------
+
+def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Nearest bf16 of float64 values, ties to even, in one rounding (bit patterns).
+
+    bf16 keeps 8 significant bits: with x = m * 2^e (0.5 <= |m| < 1, frexp), the
+    result is rint(m * 2^8) * 2^(e - 8), rint rounding half to even; both steps
+    are exact in float64.  Normal-range inputs only (the folded weights).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    r = np.ldexp(np.rint(m * 256.0), e - 8)
+    nz = r != 0
+    if np.any(np.abs(r[nz]) < 2.0 ** -126) or not np.all(np.isfinite(r)):
+        raise ValueError("outside the normal bf16 range")
+    return (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def fold_still_weight(W_bits: np.ndarray, tpatch: int, patch: int) -> np.ndarray:
+    """W' [N][3*P*P] (bf16 bits, (c, ph, pw) order): the temporal slices of W summed.
+
+    A still repeats one frame over the temporal patch (§3.2), so its T slices of
+    A are equal and  sum_s A_s W_s^T = A_0 (sum_s W_s)^T  exactly; the variant
+    stores sum_s W_s rounded once to bf16 and halves the GEMM's K.  Only that one
+    rounding differs from step 3.  The sum of bf16 values is exact in float64 and
+    is rounded to bf16 directly.
+    """
+    N = W_bits.shape[0]
+    Wf = bf16_bits_to_f64(W_bits).reshape(N, 3, tpatch, patch, patch)
+    return round_to_bf16_bits(Wf.sum(axis=2).reshape(N, 3 * patch * patch))
+
+
+def embed_folded_item(item_pixels, t, h, w, W_bits, b_bits, Wf_bits, *, patch, tpatch, merge, mean,
+                      std, rescale, still: bool) -> np.ndarray:
+    """Embeddings of one item in the folded-still variant: a still uses temporal
+    slice 0 of A against W' (fold_still_weight); a video uses step 3 unchanged."""
+    A = normalize_patchify_item(item_pixels, t, h, w, patch=patch, tpatch=tpatch, merge=merge,
+                                mean=mean, std=std, rescale=rescale)
+    if not still:
+        return embed_rows(A, W_bits, b_bits)
+    A4 = A.reshape(A.shape[0], 3, tpatch, patch * patch)
+    A0 = A4[:, :, 0, :].reshape(A.shape[0], 3 * patch * patch)
+    return embed_rows(A0, Wf_bits, b_bits)
+
+
+def embed_folded_workload(wl, bucket_rows: Optional[int] = None) -> np.ndarray:
+    Wf = fold_still_weight(wl.W_bits, wl.tpatch, wl.patch)
+    starts = _item_starts(wl.items)
+    total = int(starts[-1]) if bucket_rows is None else int(bucket_rows)
+    out = np.zeros((total, wl.hidden), dtype=np.float64)
+    for j, it in enumerate(wl.items):
+        out[starts[j]:starts[j + 1]] = embed_folded_item(
+            it.pixels, it.t, it.h, it.w, wl.W_bits, wl.b_bits, Wf, patch=wl.patch, tpatch=wl.tpatch,
+            merge=wl.merge, mean=wl.mean, std=wl.std, rescale=wl.rescale, still=(it.frames == 1))
     return out
 
 

@@ -303,6 +303,57 @@ def test_pos_ids_agree_with_patch_coords():
     assert np.array_equal(oracle.pos_ids(3, 4, 6, 2), c[:, 1:])
 
 
+# ---------------------------------------------------------------- folded-still variant
+
+def _bits(vals):
+    return np.array(vals, np.float32).view(np.uint32) >> 16
+
+
+def test_round_to_bf16_ties_to_even_and_exact_values():
+    # bf16 keeps 8 significant bits: at 1.0 the spacing is 2^-7 and 1 + 2^-8 is a tie
+    x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 2 ** -8 + 2 ** -30, -(1.0 + 3 * 2 ** -8),
+                  0.0, 2.0 ** -100, 255.0, 257.0, 0.02])
+    got = oracle.round_to_bf16_bits(x)
+    expect = [0x3F80, 0x3F80, 0x3F82, 0x3F81, 0xBF82, 0x0000, int(_bits([2.0 ** -100])[0]), 0x437F, 0x4380]
+    assert got[:9].tolist() == expect
+    # 0.02 against a brute force over the neighbouring bf16 values (nearest, then even)
+    v = 0.02
+    cands = [(abs(float(np.array([c << 16], np.uint32).view(np.float32)[0]) - v), c & 1, c)
+             for c in range(0x3C00, 0x3D00)]
+    assert int(got[9]) == min(cands)[2]
+
+
+def test_folded_weight_zero_second_slice_and_exact_sums():
+    rng = np.random.default_rng(5)
+    P, T, N = 14, 2, 6
+    K = 3 * T * P * P
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32).view(np.uint32) >> 16
+    W = W.astype(np.uint16).reshape(N, 3, T, P * P)
+    Wz = W.copy()
+    Wz[:, :, 1, :] = 0
+    # slice 1 zero: the fold is slice 0 itself, bit for bit
+    assert np.array_equal(oracle.fold_still_weight(Wz.reshape(N, K), T, P), Wz[:, :, 0, :].reshape(N, -1))
+    # equal slices: the sum doubles exactly
+    We = W.copy()
+    We[:, :, 1, :] = We[:, :, 0, :]
+    f = oracle.bf16_bits_to_f64(oracle.fold_still_weight(We.reshape(N, K), T, P))
+    assert np.array_equal(f, 2 * oracle.bf16_bits_to_f64(We[:, :, 0, :].reshape(N, -1)))
+
+
+def test_folded_embed_equals_step3_when_the_fold_is_exact():
+    # with equal weight slices the folded weight is exact, so the folded variant of a
+    # still reproduces step 3 (up to float64 summation order)
+    from vit_vision_encoder_fusedinputnorm_gb300 import synth
+    wl = synth.small_workload(8, [(1, 4, 6, 1), (1, 2, 2, 1)], patch=14, hidden=32, pixels="uniform")
+    N, K = wl.W_bits.shape
+    W = wl.W_bits.reshape(N, 3, 2, 14 * 14).copy()
+    W[:, :, 1, :] = W[:, :, 0, :]
+    wl.W_bits = W.reshape(N, K)
+    a = oracle.embed_folded_workload(wl)
+    b = oracle.embed_workload(wl)
+    assert np.allclose(a, b, rtol=0, atol=1e-12)
+
+
 # ---------------------------------------------------------------- RoPE applied to Q/K
 
 def _apply_case(seed=0, rows=7, heads=3, hd=16):
