@@ -361,6 +361,10 @@ def main():
                      None, stream)
 
     unfused_ms = timed(unfused)
+    # the folded-still variant (an approximation: the summed weight slices are rounded once
+    # to bf16), timed for reference only; it is never the headline
+    folded_ms = timed(lambda: B.vitfe_embed_folded(fe.h, batch.pixels, batch.pixel_bytes, batch.items,
+                                                   batch.n_items, batch.capacity, rows, out, None, stream))
     rope_ms = timed(lambda: B.vitfe_rope(fe.h, batch.items, batch.n_items, batch.capacity, rows, wl.head_dim,
                                          wl.theta, cos, sin, None, stream))
 
@@ -400,6 +404,9 @@ def main():
                      "kernel": "embed_kernel<14>", "flops_per_launch": flops,
                      "kernel_ms": embed_ms},
         "side_paths": {"unfused_embed_then_rope_ms": unfused_ms,
+                       "folded_still_variant": {"ms": folded_ms, "patches_per_s": world * rows / (folded_ms / 1e3),
+                                                "note": "approximation (W slices summed, rounded once to bf16); "
+                                                        "K 588 for stills; not the method's exact result"},
                        "rope_ms": rope_ms,
                        "rope_gbs": rows * wl.head_dim // 2 * 4 * 2 / (rope_ms / 1e3) / 1e9,
                        "rope_frac_hbm": rows * wl.head_dim // 2 * 4 * 2 / (rope_ms / 1e3) / 1e9 / float(pk["hbm_gbs"]),

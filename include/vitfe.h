@@ -121,6 +121,18 @@ vitfe_status vitfe_rope(vitfe_t h, const vitfe_item* items, const int32_t* n_ite
                         int32_t max_items, int64_t rows, int head_dim, float theta,
                         float* cos, float* sin, int32_t* status, cudaStream_t stream);
 
+/* Folded-still variant of vitfe_embed (NOT the method's exact result): a still's
+ * temporal slices of A are equal, so it multiplies one slice by W' = the sum of
+ * the weight's temporal slices, computed exactly and rounded once to bf16 at
+ * vitfe_create.  This halves a still's multiply-adds; only W''s rounding differs
+ * from vitfe_embed.  Tiles that hold video rows are computed exactly as by
+ * vitfe_embed.  Same arguments and conventions as vitfe_embed;
+ * VITFE_EUNSUPPORTED when tpatch == 1. */
+vitfe_status vitfe_embed_folded(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes,
+                                const vitfe_item* items, const int32_t* n_items,
+                                int32_t max_items, int64_t rows, void* out, int32_t* status,
+                                cudaStream_t stream);
+
 /* vitfe_embed and vitfe_rope over the same items in one launch: the embed
  * kernel's epilogue warps write each tile's cos/sin rows while the tile's first
  * accumulator is computed.  Arguments, outputs, pad rows and errors are those of

@@ -92,6 +92,7 @@ def test_calls_reject_null_handle(lib):
                      (B.vitfe_pos_ids, (None, 16, 16, 1, 10, 16)),
                      (B.vitfe_cu_seqlens, (None, 16, 16, 1, 10, 8, 16, 16)),
                      (B.vitfe_embed_rope, (None, 16, 100, 16, 16, 1, 10, 16, 80, 1e4, 16, 16)),
+                     (B.vitfe_embed_folded, (None, 16, 100, 16, 16, 1, 10, 16)),
                      (B.vitfe_normalize_patchify, (None, 16, 100, 16, 16, 1, 10, 16))]:
         with pytest.raises(B.VitfeError) as e:
             fn(*args)

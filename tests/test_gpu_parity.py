@@ -509,3 +509,34 @@ def test_rope_apply_vs_oracle_in_a_packed_qkv_buffer(hd, hq, hk):
     # pad rows rotate by the identity: bit-exact; everything past Q and K untouched
     assert np.array_equal(got[-5:], before[-5:])
     assert np.array_equal(got[:, (hq + hk) * hd:], before[:, (hq + hk) * hd:])
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_embed_folded_vs_folded_oracle(name):
+    # stills against the folded oracle (W' rounded once, identically on both sides); tiles
+    # holding video rows are computed unfolded, exactly as vitfe_embed computes them
+    P, N, grids = SMALL[name]
+    wl = synth.small_workload(41, grids, patch=P, hidden=N, pixels="uniform")
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    rows = b.live_rows + 100
+    st = fe.status_tensor()
+    out = fe.embed_folded(b, rows=rows, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, -1]
+    g = U.bits_to_f64(U.tensor_bits(out))
+    ref = oracle.embed_folded_workload(wl, bucket_rows=rows)
+    starts = U.item_starts(wl.items)
+    still_rows = np.zeros(rows, bool)
+    for it, s0, s1 in zip(wl.items, starts[:-1], starts[1:]):
+        still_rows[s0:s1] = it.frames == 1
+    # a 256-row tile is folded when all of its live rows are stills
+    live = b.live_rows
+    tile_all_still = np.array([t < live and still_rows[t:min(t + 256, live)].all() for t in range(0, rows, 256)])
+    folded_rows = np.repeat(tile_all_still, 256)[:rows] & still_rows
+    exact = oracle.embed_workload(wl, bucket_rows=rows)
+    expect = np.where(folded_rows[:, None], ref, exact)
+    rel, mx = U.embed_errors(g, expect, starts)
+    assert rel <= U.EMBED_REL_FROB and mx <= U.EMBED_MAX_ABS, (rel, mx)
+    assert np.all(U.tensor_bits(out)[b.live_rows:] == 0)
+    fe.close()

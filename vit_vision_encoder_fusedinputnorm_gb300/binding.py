@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "VITFE_OK", 1: "VITFE_EINVAL", 2: "VITFE_ENOMEM", 3: "VITFE_E
                 7: "VITFE_EUNSUPPORTED"}
 
 # exported symbols of include/vitfe.h
-EXPORTS = ["vitfe_create", "vitfe_destroy", "vitfe_embed", "vitfe_embed_rope", "vitfe_rope", "vitfe_normalize_patchify",
+EXPORTS = ["vitfe_create", "vitfe_destroy", "vitfe_embed", "vitfe_embed_rope", "vitfe_embed_folded", "vitfe_rope", "vitfe_normalize_patchify",
            "vitfe_pos_ids", "vitfe_cu_seqlens", "vitfe_rope_apply", "vitfe_rope_noalloc",
            "vitfe_items_from_grid",
            "vitfe_feature_dim", "vitfe_status_str"]
@@ -66,6 +66,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.vitfe_embed.restype = ctypes.c_int
     lib.vitfe_embed_rope.argtypes = [P, P, I64, P, P, I32, I64, P, ctypes.c_int, F32, P, P, P, P]
     lib.vitfe_embed_rope.restype = ctypes.c_int
+    lib.vitfe_embed_folded.argtypes = [P, P, I64, P, P, I32, I64, P, P, P]
+    lib.vitfe_embed_folded.restype = ctypes.c_int
     lib.vitfe_rope.argtypes = [P, P, P, I32, I64, ctypes.c_int, F32, P, P, P, P]
     lib.vitfe_rope.restype = ctypes.c_int
     lib.vitfe_rope_noalloc.argtypes = [ctypes.c_int, ctypes.c_int, P, P, I32, I64, ctypes.c_int, F32, P, P, P, P]
@@ -134,6 +136,13 @@ def vitfe_embed(h, pixels, pixel_bytes, items, n_items, max_items, rows, out, st
     _check("vitfe_embed", load().vitfe_embed(h, _ptr(pixels), int(pixel_bytes), _ptr(items), _ptr(n_items),
                                              int(max_items), int(rows), _ptr(out), _ptr(status),
                                              _stream(stream)))
+
+
+def vitfe_embed_folded(h, pixels, pixel_bytes, items, n_items, max_items, rows, out, status=None,
+                       stream=None) -> None:
+    _check("vitfe_embed_folded",
+           load().vitfe_embed_folded(h, _ptr(pixels), int(pixel_bytes), _ptr(items), _ptr(n_items),
+                                     int(max_items), int(rows), _ptr(out), _ptr(status), _stream(stream)))
 
 
 def vitfe_embed_rope(h, pixels, pixel_bytes, items, n_items, max_items, rows, out, head_dim, theta, cos, sin,

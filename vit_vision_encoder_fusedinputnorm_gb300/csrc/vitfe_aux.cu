@@ -676,15 +676,19 @@ size_t np_smem_bytes(int P, int T, int K, int nwr) {
 // chunk position q ^ (i & 7).  Internal feature kp of a slice is (ph*P + pw)*3 + c
 // (zero past 3*P*P); it holds canonical column ((c*T + s)*P + ph)*P + pw.
 // ---------------------------------------------------------------------------
+//
+// fold != 0 writes the folded-still weight instead: one slice whose feature holds the sum
+// of the T temporal slices' weights, taken in double (exact) and rounded once to bf16.
 __global__ void tile_weight_kernel(const __nv_bfloat16* __restrict__ W, const __nv_bfloat16* __restrict__ b,
-                                   int N, int P, int T, int nblk, int bn,
+                                   int N, int P, int T, int nblk, int bn, int fold,
                                    __nv_bfloat16* __restrict__ w_tile, float* __restrict__ bias) {
   const int kslice = 3 * P * P;
   const int K = T * kslice;
   const int bnh = bn / 2;
   const int npass = (N + bn - 1) / bn;
+  const int TL = fold ? 1 : T;                 // slices in the layout
   const long long per_blk = (long long)bnh * 64;
-  const long long total = (long long)npass * 2 * T * nblk * per_blk;
+  const long long total = (long long)npass * 2 * TL * nblk * per_blk;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
     const long long blk = idx / per_blk;
@@ -693,9 +697,9 @@ __global__ void tile_weight_kernel(const __nv_bfloat16* __restrict__ W, const __
     const int qp = (within >> 3) & 7;                 // physical chunk in the row
     const int e = ((qp ^ (i & 7)) << 3) | (within & 7);
     const int j = (int)(blk % nblk);
-    const int sl = (int)((blk / nblk) % T);
-    const int r = (int)((blk / ((long long)nblk * T)) & 1);
-    const int p = (int)(blk / ((long long)nblk * T * 2));
+    const int sl = (int)((blk / nblk) % TL);
+    const int r = (int)((blk / ((long long)nblk * TL)) & 1);
+    const int p = (int)(blk / ((long long)nblk * TL * 2));
     const int npw = min(bn, N - p * bn);
     const int kp = 64 * j + e;
     __nv_bfloat16 v = __float2bfloat16_rn(0.0f);
@@ -705,10 +709,17 @@ __global__ void tile_weight_kernel(const __nv_bfloat16* __restrict__ W, const __
       const int rem = kp - ph * 3 * P;
       const int pw = rem / 3;
       const int c = rem - pw * 3;
-      v = W[(size_t)n * K + ((c * T + sl) * P + ph) * P + pw];
+      if (fold) {
+        double acc = 0.0;
+        for (int s2 = 0; s2 < T; ++s2) acc += (double)__bfloat162float(W[(size_t)n * K + ((c * T + s2) * P + ph) * P + pw]);
+        v = __double2bfloat16(acc);
+      } else {
+        v = W[(size_t)n * K + ((c * T + sl) * P + ph) * P + pw];
+      }
     }
     w_tile[idx] = v;
   }
+  if (fold) return;
   for (long long n = (long long)blockIdx.x * blockDim.x + threadIdx.x; n < N; n += (long long)gridDim.x * blockDim.x)
     bias[n] = b ? __bfloat162float(b[n]) : 0.0f;
 }
@@ -822,7 +833,12 @@ cudaError_t launch_normalize_patchify(const Ctx& c, const uint8_t* pixels, int64
 cudaError_t launch_tile_weight(const Ctx& c, const __nv_bfloat16* W, const __nv_bfloat16* b, cudaStream_t s) {
   const long long total = (long long)c.w_tile_bytes / 2;
   const int grid = grid_for(total, 256, c.sm_count * 16);
-  tile_weight_kernel<<<grid, 256, 0, s>>>(W, b, c.N, c.P, c.T, c.nblk, c.bn, c.w_tile, c.bias);
+  tile_weight_kernel<<<grid, 256, 0, s>>>(W, b, c.N, c.P, c.T, c.nblk, c.bn, 0, c.w_tile, c.bias);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || c.w_tile_f == nullptr) return e;
+  const long long total_f = (long long)c.w_tile_f_bytes / 2;
+  tile_weight_kernel<<<grid_for(total_f, 256, c.sm_count * 16), 256, 0, s>>>(W, b, c.N, c.P, c.T, c.nblk, c.bn, 1,
+                                                                            c.w_tile_f, c.bias);
   return cudaGetLastError();
 }
 

@@ -69,6 +69,7 @@ struct EmbedArgs {
   float* rope_cos;
   float* rope_sin;
   int rope_nf;             // head_dim / 4
+  int folded;              // still tiles multiply one slice of A by the folded-still weight
 };
 
 // Shared-memory header (placed before the 1024-aligned tile area).
@@ -393,7 +394,8 @@ __device__ __forceinline__ void prefetch_row(const RowSrc& src, int nslices) {
 
 template <int P>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    embed_kernel(const __grid_constant__ CUtensorMap tmap_w, const EmbedArgs args) {
+    embed_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_wf,
+                 const EmbedArgs args) {
   constexpr int KS = 3 * P * P;
   constexpr int NBLK = (KS + 63) / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -440,7 +442,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_alloc_pair(smem_u32(&hs->tmem_base), (uint32_t)args.tmem_cols);
     tmem_relinquish_pair();
   }
-  if (warp == kTmaWarp && lane == 0) tma_prefetch_desc(&tmap_w);
+  if (warp == kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&tmap_w);
+    if (args.folded) tma_prefetch_desc(&tmap_wf);
+  }
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
@@ -494,19 +499,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int tile = cid; ok && tile < args.num_tiles; tile += ncl) {
         const int kind = tile_kind(tile * kPairRows, hs, args.T);
         if (kind == kPad) continue;
-        const int nsteps = args.T * NBLK;
+        // folded still tiles: one slice of the folded weight per block
+        const bool fold = args.folded && kind == kResident;
+        const int Ts = fold ? 1 : args.T;
+        const CUtensorMap* map = fold ? &tmap_wf : &tmap_w;
+        const int nsteps = Ts * NBLK;
         for (int p = 0; ok && p < args.npass; ++p) {
           // this CTA's images of pass p: (p, rank, slice, block), bnh/4 rows of 512 B each
-          const int blk0 = (p * 2 + (int)rank) * args.T * NBLK;
+          const int blk0 = (p * 2 + (int)rank) * Ts * NBLK;
           for (int st = 0; ok && st < nsteps; ++st) {
-            const int j = blk_order<NBLK>((kind == kResident) ? st / args.T : st % NBLK);
-            const int sl = (kind == kResident) ? st % args.T : st / NBLK;
+            const int j = blk_order<NBLK>((kind == kResident) ? st / Ts : st % NBLK);
+            const int sl = (kind == kResident) ? st % Ts : st / NBLK;
             if (!mbar_wait_cl(smem_u32(&hs->b_empty[stage]), bphase ^ 1u, abort_flag, args.limit_ns)) {
               ok = false;
               break;
             }
             if (leader) mbar_arrive_expect_tx(smem_u32(&hs->b_full[stage]), 2u * b_stage_bytes);
-            tma_load_2d_pair(b_smem + stage * b_stage_bytes, &tmap_w, b_full_L + 8u * stage, 0,
+            tma_load_2d_pair(b_smem + stage * b_stage_bytes, map, b_full_L + 8u * stage, 0,
                              (blk0 + sl * NBLK + j) * (bnh / 4));
             ++nb;
             if (++stage == (uint32_t)args.nstage) { stage = 0; bphase ^= 1u; }
@@ -594,13 +603,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t idesc = idesc_bf16(kPairRows, npw);
           const uint32_t d_tmem = tmem + buf * (uint32_t)args.bn;
           if (kind == kResident) {
-            // one resident slice of A feeds every temporal slice of W
+            // one resident slice of A feeds every temporal slice of W (one folded slice)
+            const int Ts = args.folded ? 1 : T;
 #pragma unroll
             for (int jj = 0; jj < NBLK; ++jj) {
               const int j = blk_order<NBLK>(jj);
               if (p == 0) VITFE_WAIT_A(j);
               const uint64_t ad = adesc0 + (uint64_t)(j * (kABlockBytes >> 4));
-              for (int sl = 0; ok && sl < T; ++sl) {
+              for (int sl = 0; ok && sl < Ts; ++sl) {
                 VITFE_WAIT_B();
                 if (!ok) break;
                 VITFE_STEP(ad, ksteps_of<P>(j), j == 0 && sl == 0);
@@ -795,7 +805,7 @@ cudaError_t embed_configure(Ctx& c) {
 cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_bytes,
                          const vitfe_item* items, const int32_t* n_items, int max_items,
                          int64_t rows, void* out, int32_t* status, cudaStream_t s, const float* rope_tab,
-                         int rope_nf, float* rope_cos, float* rope_sin) {
+                         int rope_nf, float* rope_cos, float* rope_sin, bool folded) {
   EmbedArgs a;
   a.pixels = pixels;
   a.pixel_bytes = pixel_bytes;
@@ -822,13 +832,14 @@ cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_byte
   a.rope_cos = rope_cos;
   a.rope_sin = rope_sin;
   a.rope_nf = rope_nf;
+  a.folded = folded ? 1 : 0;
   int pairs = a.num_tiles < c.max_clusters ? a.num_tiles : c.max_clusters;
   if (pairs < 1) pairs = 1;
   const int grid = 2 * pairs;
   if (c.P == 14)
-    embed_kernel<14><<<grid, kThreads, c.embed_smem, s>>>(c.tmap_w, a);
+    embed_kernel<14><<<grid, kThreads, c.embed_smem, s>>>(c.tmap_w, c.tmap_wf, a);
   else
-    embed_kernel<16><<<grid, kThreads, c.embed_smem, s>>>(c.tmap_w, a);
+    embed_kernel<16><<<grid, kThreads, c.embed_smem, s>>>(c.tmap_w, c.tmap_wf, a);
   return cudaGetLastError();
 }
 

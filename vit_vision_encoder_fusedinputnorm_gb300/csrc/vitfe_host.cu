@@ -37,6 +37,7 @@ constexpr int64_t kMaxRows = 0x7fffffffLL - 1024;
 void free_ctx(vitfe_ctx* h) {
   if (!h) return;
   if (h->c.w_tile) cudaFree(h->c.w_tile);
+  if (h->c.w_tile_f) cudaFree(h->c.w_tile_f);
   if (h->c.bias) cudaFree(h->c.bias);
   if (h->c.rope_tab) cudaFree(h->c.rope_tab);
   delete h;
@@ -128,7 +129,9 @@ vitfe_status vitfe_create(vitfe_t* out, const float mean[3], const float std_[3]
   if (c.embed_ok) {
     const size_t npass = (size_t)((c.N + c.bn - 1) / c.bn);
     c.w_tile_bytes = npass * 2 * (size_t)c.T * (size_t)c.nblk * (size_t)(c.bn / 2) * 128;
-    if (cudaMalloc(&c.w_tile, c.w_tile_bytes) != cudaSuccess) {
+    c.w_tile_f_bytes = c.T > 1 ? c.w_tile_bytes / (size_t)c.T : 0;
+    if (cudaMalloc(&c.w_tile, c.w_tile_bytes) != cudaSuccess ||
+        (c.w_tile_f_bytes > 0 && cudaMalloc(&c.w_tile_f, c.w_tile_f_bytes) != cudaSuccess)) {
       cudaGetLastError();
       free_ctx(h);
       return VITFE_ENOMEM;
@@ -154,6 +157,12 @@ vitfe_status vitfe_create(vitfe_t* out, const float mean[3], const float std_[3]
     CUresult r = enc(&c.tmap_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.w_tile, gdim, gstride, box, estride,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS && c.w_tile_f != nullptr) {
+      const cuuint64_t gdim_f[2] = {256u, (cuuint64_t)(c.w_tile_f_bytes / 512)};
+      r = enc(&c.tmap_wf, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.w_tile_f, gdim_f, gstride, box, estride,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS) {
       free_ctx(h);
       return VITFE_ECUDA;
@@ -180,6 +189,19 @@ vitfe_status vitfe_embed(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes, 
   if (!h->c.embed_ok) return VITFE_EUNSUPPORTED;
   return from_cuda(vitfe::launch_embed(h->c, pixels, pixel_bytes, items, n_items, max_items, rows, out, status,
                                        stream));
+}
+
+vitfe_status vitfe_embed_folded(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes, const vitfe_item* items,
+                                const int32_t* n_items, int32_t max_items, int64_t rows, void* out,
+                                int32_t* status, cudaStream_t stream) {
+  vitfe_status st = check_common(h, items, n_items, max_items, rows);
+  if (st != VITFE_OK) return st;
+  if (pixels == nullptr || pixel_bytes < 0 || !aligned(pixels, 16)) return VITFE_EINVAL;
+  if ((out == nullptr && rows > 0) || !aligned(out, 16)) return VITFE_EINVAL;
+  if (status && !aligned(status, 4)) return VITFE_EINVAL;
+  if (!h->c.embed_ok || h->c.w_tile_f == nullptr) return VITFE_EUNSUPPORTED;
+  return from_cuda(vitfe::launch_embed(h->c, pixels, pixel_bytes, items, n_items, max_items, rows, out, status,
+                                       stream, nullptr, 0, nullptr, nullptr, true));
 }
 
 vitfe_status vitfe_embed_rope(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes, const vitfe_item* items,

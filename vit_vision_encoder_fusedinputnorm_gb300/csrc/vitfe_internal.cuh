@@ -31,6 +31,8 @@ struct Ctx {
   int K = 0;           // 3 * T * P * P (canonical feature width)
   __nv_bfloat16* w_tile = nullptr; // W as the embed kernel's shared-memory images (tile_weight_kernel)
   size_t w_tile_bytes = 0;
+  __nv_bfloat16* w_tile_f = nullptr;  // folded-still weight images (one slice: sum of the T slices)
+  size_t w_tile_f_bytes = 0;
   float* bias = nullptr;           // [N] fp32 (zeros when no bias)
   // RoPE axis tables (the cos/sin cache), one slot per (head_dim, theta) seen, each
   // [2][VITFE_ROPE_MAX_SIDE][head_dim/4] fp32 covering every position, built on first use
@@ -47,6 +49,7 @@ struct Ctx {
   bool rope_built[kRopeSlots] = {false, false, false, false};
   int rope_used = 0;               // slots holding a key
   CUtensorMap tmap_w;              // w_tile viewed as 512-byte rows; a box is one image (bn/8 rows)
+  CUtensorMap tmap_wf;             // the same over w_tile_f
   int bn = 0;                      // GEMM N tile of a CTA pair (<= 256)
   int nstage = 0;                  // B pipeline stages
   int max_clusters = 0;            // co-resident CTA pairs of the embed kernel
@@ -499,11 +502,12 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
 // ---------------------------------------------------------------------------
 // rope_cos != nullptr: the same launch also writes the 2D-RoPE rows from rope_tab
 // (an axis table from rope_table_for; nf = head_dim / 4).
+// folded: still tiles use the folded-still weight (one slice of K).
 cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_bytes,
                          const vitfe_item* items, const int32_t* n_items, int max_items,
                          int64_t rows, void* out, int32_t* status, cudaStream_t s,
                          const float* rope_tab = nullptr, int rope_nf = 0, float* rope_cos = nullptr,
-                         float* rope_sin = nullptr);
+                         float* rope_sin = nullptr, bool folded = false);
 cudaError_t embed_configure(Ctx& c);
 // The handle's cos/sin axis table of (head_dim, theta): found in its slots, or built there
 // (one launch on `s`) the first time.  Layout: cos at [p * nf + i], sin at

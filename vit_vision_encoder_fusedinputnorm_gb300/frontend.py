@@ -98,6 +98,16 @@ class FrontEnd:
                                    status, self._stream(stream))
         return out
 
+    def embed_folded(self, b: Batch, rows: Optional[int] = None, out=None, status=None, stream=None):
+        """The folded-still variant of embed (an approximation; see vitfe_embed_folded)."""
+        torch = self.torch
+        rows = b.live_rows if rows is None else rows
+        if out is None:
+            out = torch.empty((rows, self.hidden), dtype=torch.bfloat16, device=self.device)
+        B.vitfe_embed_folded(self.h, b.pixels, b.pixel_bytes, b.items, b.n_items, b.capacity, rows, out, status,
+                             self._stream(stream))
+        return out
+
     def embed_rope(self, b: Batch, head_dim: int, theta: float, rows: Optional[int] = None, out=None, cos=None,
                    sin=None, status=None, stream=None):
         """embed + rope in one launch: (out, cos, sin)."""
