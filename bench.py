@@ -185,6 +185,7 @@ def kernel_only(args):
     from vit_vision_encoder_fusedinputnorm_gb300 import build as vbuild
     from vit_vision_encoder_fusedinputnorm_gb300 import synth
     from vit_vision_encoder_fusedinputnorm_gb300.frontend import FrontEnd
+    from vit_vision_encoder_fusedinputnorm_gb300 import binding as B
     vbuild.build()
     wl = synth.make_workload(CFG, item_subset=list(range(args.images)))
     wl.items = wl.items[:args.images]
@@ -195,9 +196,21 @@ def kernel_only(args):
     for i in range(args.warmup + args.launches):
         if args.kernel_only == "embed":
             bufs["o"] = fe.embed(b, out=bufs.get("o"), status=st)
+        elif args.kernel_only == "embed_rope":
+            o, c, s_ = fe.embed_rope(b, wl.head_dim, wl.theta, out=bufs.get("o"), cos=bufs.get("c"),
+                                     sin=bufs.get("s"), status=st)
+            bufs["o"], bufs["c"], bufs["s"] = o, c, s_
         elif args.kernel_only == "rope":
             c, s_ = fe.rope(b, wl.head_dim, wl.theta, cos=bufs.get("c"), sin=bufs.get("s"), status=st)
             bufs["c"], bufs["s"] = c, s_
+        elif args.kernel_only == "rope_apply":
+            if "qkv" not in bufs:
+                bufs["c"], bufs["s"] = fe.rope(b, wl.head_dim, wl.theta, status=st)
+                bufs["qkv"] = torch.zeros((b.live_rows, 3 * wl.hidden), dtype=torch.bfloat16, device="cuda")
+            heads = wl.hidden // wl.head_dim
+            q = bufs["qkv"]
+            B.vitfe_rope_apply(bufs["c"], bufs["s"], b.live_rows, wl.head_dim, q, heads, 3 * wl.hidden,
+                               q[:, wl.hidden:], heads, 3 * wl.hidden)
         else:
             bufs["o"] = fe.normalize_patchify(b, out=bufs.get("o"), status=st)
     torch.cuda.synchronize()
@@ -215,7 +228,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-only", choices=["embed", "rope", "normalize_patchify"],
+    ap.add_argument("--kernel-only", choices=["embed", "embed_rope", "rope", "rope_apply", "normalize_patchify"],
                     help="profiling mode: launch one entry point on a subset of the images, print nothing")
     ap.add_argument("--images", type=int, default=64, help="images of the workload (profiling mode)")
     ap.add_argument("--launches", type=int, default=3, help="launches after warm-up (profiling mode)")
