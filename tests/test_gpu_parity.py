@@ -476,8 +476,9 @@ def test_embed_rope_graph_replay_with_new_items():
     fe.close()
 
 
-@pytest.mark.parametrize("hd,hq,hk", [(80, 16, 16), (72, 3, 5), (64, 2, 0), (8, 0, 3), (16, 1, 1)])
-def test_rope_apply_vs_oracle_in_a_packed_qkv_buffer(hd, hq, hk):
+@pytest.mark.parametrize("pad", [4, 0])           # 4: 8-byte accesses; 0: 16-byte accesses where aligned
+@pytest.mark.parametrize("hd,hq,hk", [(80, 16, 16), (72, 3, 5), (64, 2, 0), (8, 0, 3), (16, 1, 1), (32, 3, 2)])
+def test_rope_apply_vs_oracle_in_a_packed_qkv_buffer(hd, hq, hk, pad):
     # Q and K are views into [rows][Q | K | V]; V and the padding must stay untouched
     from vit_vision_encoder_fusedinputnorm_gb300 import binding as B
     rng = np.random.default_rng(hd + hq)
@@ -486,7 +487,7 @@ def test_rope_apply_vs_oracle_in_a_packed_qkv_buffer(hd, hq, hk):
     pos[-5:] = -1                                       # a few bucket-pad rows (identity)
     c64, s64 = oracle.rope_tables(pos, hd, 10000.0)
     c32, s32 = c64.astype(np.float32), s64.astype(np.float32)
-    width = (hq + hk + 2) * hd + 4                      # + V heads and 4 elements of padding
+    width = (hq + hk + 2) * hd + pad                    # + V heads and the padding
     x = rng.standard_normal((rows, width)).astype(np.float32)
     xb = torch.from_numpy(x).to(torch.bfloat16)
     before = U.tensor_bits(xb)

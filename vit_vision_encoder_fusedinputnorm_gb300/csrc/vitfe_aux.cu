@@ -53,8 +53,8 @@ __global__ void __launch_bounds__(kAuxThreads) pos_ids_kernel(const vitfe_item* 
 // per head, feature i and feature i + hh (hh = head_dim / 2) rotate as one pair by the
 // angle of table column i:  y[i] = x[i] c - x[i+hh] s,  y[i+hh] = x[i+hh] c + x[i] s,
 // c = cos[r][i], s = sin[r][i]; fp32 arithmetic, bf16 round-to-nearest-even, in place.
-// One warp per row at a time; lane units are (head, group of 4 pairs) of the row, Q heads
-// first, walked 32 at a time without division.
+// One warp per row at a time; lane units are (head, group of V pairs) of the row, Q heads
+// first, walked without division.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void bf16x4_to_f32(uint2 v, float* f) {
   f[0] = __uint_as_float(v.x << 16);
@@ -68,47 +68,97 @@ __device__ __forceinline__ uint2 f32_to_bf16x4(const float* f) {
   return make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
 }
 
+// V pairs of one head half (V = 4: 8-byte accesses, V = 8: 16-byte accesses).
+template <int V>
+struct ApplyVec;
+template <>
+struct ApplyVec<4> {
+  using X = uint2;
+  __device__ static void load_tab(const float* p, float* f) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+  }
+  __device__ static void unpack(X v, float* f) { bf16x4_to_f32(v, f); }
+  __device__ static X pack(const float* f) { return f32_to_bf16x4(f); }
+};
+template <>
+struct ApplyVec<8> {
+  using X = uint4;
+  __device__ static void load_tab(const float* p, float* f) {
+    ApplyVec<4>::load_tab(p, f);
+    ApplyVec<4>::load_tab(p + 4, f + 4);
+  }
+  __device__ static void unpack(X v, float* f) {
+    bf16x4_to_f32(make_uint2(v.x, v.y), f);
+    bf16x4_to_f32(make_uint2(v.z, v.w), f + 4);
+  }
+  __device__ static X pack(const float* f) {
+    const uint2 a = f32_to_bf16x4(f), b = f32_to_bf16x4(f + 4);
+    return make_uint4(a.x, a.y, b.x, b.y);
+  }
+};
+
+// Lane units are (head, group of V pairs); each lane takes NB units per step (u, u + 32,
+// ...) and issues all their Q/K loads before any table load or arithmetic.
+template <int V, int NB>
 __global__ void __launch_bounds__(kAuxThreads) rope_apply_kernel(const float* __restrict__ cos,
                                                                  const float* __restrict__ sin, int rows, int hh,
                                                                  int heads_q, int heads_k, __nv_bfloat16* q,
                                                                  long long q_stride, __nv_bfloat16* k,
                                                                  long long k_stride) {
+  using AV = ApplyVec<V>;
+  using X = typename AV::X;
   const int lane = threadIdx.x & 31;
   const int gw = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
   const int nw = (int)((gridDim.x * (unsigned)blockDim.x) >> 5);
-  const int G = hh >> 2;                       // groups of 4 pairs per head
+  const int G = hh / V;                        // groups of V pairs per head
   const int units = (heads_q + heads_k) * G;   // per row
   const int h0 = lane / G, j0 = lane - h0 * G;
   const int dh = 32 / G, dj = 32 - dh * G;     // a step of 32 units in (head, group)
   for (int r = gw; r < rows; r += nw) {
     const float* cr = cos + (size_t)r * hh;
     const float* sr = sin + (size_t)r * hh;
+    __nv_bfloat16* qr = q + (size_t)r * q_stride;
+    __nv_bfloat16* kr = k + (size_t)r * k_stride;
     int hd = h0, j = j0;
-#pragma unroll 2
-    for (int u = lane; u < units; u += 32) {
-      __nv_bfloat16* x = (hd < heads_q) ? q + (size_t)r * q_stride + (size_t)hd * (2 * hh)
-                                        : k + (size_t)r * k_stride + (size_t)(hd - heads_q) * (2 * hh);
-      uint2* p1 = reinterpret_cast<uint2*>(x + 4 * j);
-      uint2* p2 = reinterpret_cast<uint2*>(x + hh + 4 * j);
-      const float4 c4 = __ldg(reinterpret_cast<const float4*>(cr + 4 * j));
-      const float4 s4 = __ldg(reinterpret_cast<const float4*>(sr + 4 * j));
-      float a[4], b[4], ya[4], yb[4];
-      bf16x4_to_f32(*p1, a);
-      bf16x4_to_f32(*p2, b);
-      const float c[4] = {c4.x, c4.y, c4.z, c4.w};
-      const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
+    for (int u = lane; u < units; u += 32 * NB) {
+      X* p1[NB];
+      X* p2[NB];
+      int jj[NB];
+      X v1[NB], v2[NB];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        ya[e] = fmaf(a[e], c[e], -(b[e] * sn[e]));
-        yb[e] = fmaf(b[e], c[e], a[e] * sn[e]);
+      for (int b = 0; b < NB; ++b) {
+        const bool live = u + 32 * b < units;
+        __nv_bfloat16* x = (hd < heads_q) ? qr + (size_t)hd * (2 * hh) : kr + (size_t)(hd - heads_q) * (2 * hh);
+        p1[b] = reinterpret_cast<X*>(x + V * j);
+        p2[b] = reinterpret_cast<X*>(x + hh + V * j);
+        jj[b] = j;
+        if (live) {
+          v1[b] = *p1[b];
+          v2[b] = *p2[b];
+          hd += dh;
+          j += dj;
+          if (j >= G) {
+            j -= G;
+            ++hd;
+          }
+        }
       }
-      *p1 = f32_to_bf16x4(ya);
-      *p2 = f32_to_bf16x4(yb);
-      hd += dh;
-      j += dj;
-      if (j >= G) {
-        j -= G;
-        ++hd;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (u + 32 * b >= units) break;
+        float c[V], sn[V], a1[V], a2[V], y1[V], y2[V];
+        AV::load_tab(cr + V * jj[b], c);
+        AV::load_tab(sr + V * jj[b], sn);
+        AV::unpack(v1[b], a1);
+        AV::unpack(v2[b], a2);
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          y1[e] = fmaf(a1[e], c[e], -(a2[e] * sn[e]));
+          y2[e] = fmaf(a2[e], c[e], a1[e] * sn[e]);
+        }
+        *p1[b] = AV::pack(y1);
+        *p2[b] = AV::pack(y2);
       }
     }
   }
@@ -744,9 +794,19 @@ cudaError_t launch_rope_apply(const float* cos, const float* sin, int64_t rows, 
   if (e != cudaSuccess) return e;
   const int warps_per_cta = kAuxThreads / 32;
   const int grid = grid_for(rows, warps_per_cta, sms * 8);
-  rope_apply_kernel<<<grid, kAuxThreads, 0, s>>>(cos, sin, (int)rows, head_dim / 2, heads_q, heads_k,
-                                                 static_cast<__nv_bfloat16*>(q), q_stride,
-                                                 static_cast<__nv_bfloat16*>(k), k_stride);
+  // 16-byte accesses when every head half and row start is 16-byte aligned
+  const int hh = head_dim / 2;
+  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  const bool v8 = (hh % 8) == 0 && (heads_q == 0 || (a16(q) && q_stride % 8 == 0)) &&
+                  (heads_k == 0 || (a16(k) && k_stride % 8 == 0));
+  if (v8)
+    rope_apply_kernel<8, 4><<<grid, kAuxThreads, 0, s>>>(cos, sin, (int)rows, hh, heads_q, heads_k,
+                                                      static_cast<__nv_bfloat16*>(q), q_stride,
+                                                      static_cast<__nv_bfloat16*>(k), k_stride);
+  else
+    rope_apply_kernel<4, 4><<<grid, kAuxThreads, 0, s>>>(cos, sin, (int)rows, hh, heads_q, heads_k,
+                                                      static_cast<__nv_bfloat16*>(q), q_stride,
+                                                      static_cast<__nv_bfloat16*>(k), k_stride);
   return cudaGetLastError();
 }
 
