@@ -507,10 +507,11 @@ __global__ void __launch_bounds__(kAuxThreads) normalize_patchify_kernel(const N
 // a time, end to end: lanes 0-1 decode the rows, one lane per (row, pixel row ph) loads the
 // 3P-byte run of each stored frame once (aligned 4-byte loads) and writes, for every channel
 // c and temporal slice t, the P features (c, t, ph, 0..P-1) of the canonical order into the
-// warp's shared-memory copy of the two rows, which the warp then writes out with contiguous
-// 16-byte stores (the rows are adjacent in the output).  The loads of the warp's next pair
-// are issued before the current pair is converted, so every warp keeps one pair of pixel
-// runs in flight while it converts and writes; there is no CTA-wide barrier in the loop.
+// warp's shared-memory copy of the two rows, which the TMA engine then writes out with one
+// bulk copy per row (keeping the copy-out off the load/store pipe, which the pixel loads
+// and stage writes keep busy).  The loads of the warp's next pair are issued before the
+// current pair is converted, so every warp keeps one pair of pixel runs in flight while it
+// converts; there is no CTA-wide barrier in the loop.
 constexpr int kNpWarpRows = 2;
 
 // Two fp32 lanes in one 64-bit register (packed f32x2 arithmetic, exact per lane).
@@ -635,6 +636,21 @@ __device__ __forceinline__ void np_convert(const NpPair<P, T>& q, uint32_t* srow
   }
 }
 
+// Bulk asynchronous copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory to global memory, by the TMA engine.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every committed bulk store has finished reading its shared-memory source
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// every committed bulk store is complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 template <int P, int T>
 __global__ void __launch_bounds__(kAuxThreads) normalize_patchify_p_kernel(const NpArgs a) {
   constexpr int KW = 3 * T * P * P / 2;                     // bf16 pairs per row
@@ -664,19 +680,23 @@ __global__ void __launch_bounds__(kAuxThreads) normalize_patchify_p_kernel(const
     const int rn = rb + step;
     NpPair<P, T> nxt;
     if (rn < a.rows) np_fetch<P, T>(nxt, a, st, rn, lane);
+    // the previous pair's bulk stores must have read the stage before it is rewritten
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
     if (lr < cur.nrows) np_convert<P, T>(cur, stage + lr * RS, ph, sc, sh);
+    // each row goes out as one bulk copy by the TMA engine, off the load/store pipe
+    fence_proxy_async_smem();
     __syncwarp();
-    // the two rows are adjacent in the output: write them with 16-byte stores
-    constexpr int KW4 = KW / 4, GAP4 = (RS - KW) / 4;
-    const int nvec = cur.nrows * KW4;
-    uint4* dst = reinterpret_cast<uint4*>(a.out) + (size_t)rb * KW4;
-    const uint4* src = reinterpret_cast<const uint4*>(stage);
-    for (int v = lane; v < nvec; v += 32) __stcs(dst + v, src[v + (v >= KW4 ? GAP4 : 0)]);
-    __syncwarp();
+    if (lane == 0) {
+      for (int row = 0; row < cur.nrows; ++row)
+        bulk_store(a.out + (size_t)(rb + row) * (2 * KW), stage + row * RS, (uint32_t)(KW * 4));
+      bulk_commit();
+    }
     if (rn >= a.rows) break;
     cur = nxt;
     rb = rn;
   }
+  if (lane == 0) bulk_wait_all();
 }
 
 int grid_for(long long work, int per_cta, int cap) {
