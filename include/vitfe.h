@@ -48,6 +48,7 @@ extern "C" {
 #define VITFE_MAX_ITEMS 256      /* items per call (max_items bound)            */
 #define VITFE_ROPE_MAX_SIDE 4096 /* largest h or w (in patches) vitfe_rope takes */
 #define VITFE_ROPE_MAX_HEAD_DIM 512
+#define VITFE_MAX_HOST_ITEMS 65536 /* items per vitfe_embed_rope_host call         */
 
 typedef struct vitfe_ctx* vitfe_t;
 
@@ -120,6 +121,25 @@ vitfe_status vitfe_embed(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes,
 vitfe_status vitfe_rope(vitfe_t h, const vitfe_item* items, const int32_t* n_items,
                         int32_t max_items, int64_t rows, int head_dim, float theta,
                         float* cos, float* sin, int32_t* status, cudaStream_t stream);
+
+/* vitfe_embed_rope from HOST buffers, with the copies overlapped: the items are cut
+ * into `chunks` runs of consecutive items with about equal rows (at most
+ * VITFE_MAX_ITEMS items each); each run's pixels and descriptors go up, the fused
+ * launch runs and its results come down on three streams of the handle, so one
+ * run's upload and launch overlap the previous run's download.
+ * pixels (host, pixel_bytes), items (host, n_items <= VITFE_MAX_HOST_ITEMS): as
+ *   for vitfe_embed, but validated on the host (every item's pixels must lie
+ *   inside the buffer; otherwise VITFE_EINVAL and nothing is copied).
+ * out (host bf16 [rows][hidden]), cos, sin (host fp32 [rows][head_dim/2]),
+ *   rows = sum of t*h*w (no bucket padding); status (host int32[2], optional):
+ *   the first device error, its item index counted over all items.
+ * Page-locked host memory is what lets the copies overlap.  The handle keeps
+ * device staging for two runs (grown on demand, freed by vitfe_destroy).
+ * Returns when every result is in host memory.  Not capturable. */
+vitfe_status vitfe_embed_rope_host(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes,
+                                   const vitfe_item* items, int32_t n_items, void* out,
+                                   int head_dim, float theta, float* cos, float* sin,
+                                   int32_t* status, int32_t chunks);
 
 /* Folded-still variant of vitfe_embed (NOT the method's exact result): a still's
  * temporal slices of A are equal, so it multiplies one slice by W' = the sum of

@@ -541,3 +541,57 @@ def test_embed_folded_vs_folded_oracle(name):
     assert rel <= U.EMBED_REL_FROB and mx <= U.EMBED_MAX_ABS, (rel, mx)
     assert np.all(U.tensor_bits(out)[b.live_rows:] == 0)
     fe.close()
+
+
+@pytest.mark.parametrize("chunks", [1, 2, 3, 7])
+@pytest.mark.parametrize("name", ["mixed_p14", "stills_p16", "video_p14"])
+def test_embed_rope_host_pipeline_equals_the_device_call(name, chunks):
+    # host buffers in and out, the items cut into overlapped runs.  The RoPE rows equal the
+    # device-buffer call's bit for bit; the embeddings meet the oracle bars (a run boundary
+    # changes which rows share a 256-row tile, and with it the K summation order of stills
+    # between the resident and stream paths, so bits may differ from the one-call result)
+    P, N, grids = SMALL[name]
+    hd = 80 if P == 14 else 72
+    wl = synth.small_workload(51, grids, patch=P, hidden=N, head_dim=hd, pixels="uniform")
+    fe = _fe(wl)
+    out, cos, sin, st = fe.embed_rope_host(wl.items, hd, wl.theta, chunks=chunks)
+    assert st.tolist() == [0, -1]
+    b = fe.upload(wl.items)
+    o2, c2, s2 = fe.embed_rope(b, hd, wl.theta)
+    torch.cuda.synchronize()
+    assert np.array_equal(cos.numpy(), c2.cpu().numpy()) and np.array_equal(sin.numpy(), s2.cpu().numpy())
+    ref = oracle.embed_workload(wl)
+    rel, mx = U.embed_errors(U.bits_to_f64(U.tensor_bits(out)), ref, U.item_starts(wl.items))
+    assert rel <= U.EMBED_REL_FROB and mx <= U.EMBED_MAX_ABS, (rel, mx)
+    if chunks == 1:
+        assert np.array_equal(U.tensor_bits(out), U.tensor_bits(o2))
+    fe.close()
+
+
+def test_embed_rope_host_reports_errors():
+    from vit_vision_encoder_fusedinputnorm_gb300 import binding as B
+    wl = synth.small_workload(52, [(1, 4, 6, 1), (1, 2, 2, 1), (1, 6, 4, 1)], patch=14, hidden=256, head_dim=80)
+    fe = _fe(wl)
+    items, buf, rows = B.pack_items(wl.items, 14, 2)
+    out = np.zeros((rows, 256), np.uint16)
+    cos = np.zeros((rows, 40), np.float32)
+    sin = np.zeros((rows, 40), np.float32)
+    st = np.zeros(2, np.int32)
+    # pixels past the host buffer: rejected on the host, nothing copied
+    with pytest.raises(B.VitfeError) as e:
+        B.vitfe_embed_rope_host(fe.h, buf, buf.size - 16, items.view(np.uint8), len(items), out, 80, 1e4, cos, sin,
+                                st, 2)
+    assert e.value.code == 1
+    # a descriptor only the device rejects (w not a multiple of the merge size): reported
+    # with its index over all items, its rows zero, the others intact
+    bad = items.copy()
+    bad["w"][2] = 3
+    bad["t"][2] = 1
+    rows_bad = int(np.sum(bad["t"] * bad["h"] * bad["w"]))
+    out = np.zeros((rows_bad, 256), np.uint16)
+    cos = np.zeros((rows_bad, 40), np.float32)
+    sin = np.zeros((rows_bad, 40), np.float32)
+    B.vitfe_embed_rope_host(fe.h, buf, buf.size, bad.view(np.uint8), len(bad), out, 80, 1e4, cos, sin, st, 3)
+    assert st.tolist() == [4, 2]
+    assert np.all(out[rows_bad - 6 * 3:] == 0)
+    fe.close()

@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "VITFE_OK", 1: "VITFE_EINVAL", 2: "VITFE_ENOMEM", 3: "VITFE_E
                 7: "VITFE_EUNSUPPORTED"}
 
 # exported symbols of include/vitfe.h
-EXPORTS = ["vitfe_create", "vitfe_destroy", "vitfe_embed", "vitfe_embed_rope", "vitfe_embed_folded", "vitfe_rope", "vitfe_normalize_patchify",
+EXPORTS = ["vitfe_create", "vitfe_destroy", "vitfe_embed", "vitfe_embed_rope", "vitfe_embed_rope_host",
+           "vitfe_embed_folded", "vitfe_rope", "vitfe_normalize_patchify",
            "vitfe_pos_ids", "vitfe_cu_seqlens", "vitfe_rope_apply", "vitfe_rope_noalloc",
            "vitfe_items_from_grid",
            "vitfe_feature_dim", "vitfe_status_str"]
@@ -66,6 +67,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.vitfe_embed.restype = ctypes.c_int
     lib.vitfe_embed_rope.argtypes = [P, P, I64, P, P, I32, I64, P, ctypes.c_int, F32, P, P, P, P]
     lib.vitfe_embed_rope.restype = ctypes.c_int
+    lib.vitfe_embed_rope_host.argtypes = [P, P, I64, P, I32, P, ctypes.c_int, F32, P, P, P, I32]
+    lib.vitfe_embed_rope_host.restype = ctypes.c_int
     lib.vitfe_embed_folded.argtypes = [P, P, I64, P, P, I32, I64, P, P, P]
     lib.vitfe_embed_folded.restype = ctypes.c_int
     lib.vitfe_rope.argtypes = [P, P, P, I32, I64, ctypes.c_int, F32, P, P, P, P]
@@ -97,6 +100,15 @@ def _ptr(x) -> Optional[int]:
         return None
     if isinstance(x, int):
         return x
+    return int(x.data_ptr())
+
+
+def _hptr(x) -> Optional[int]:
+    """Address of a host buffer: numpy array, torch CPU tensor, int, or None."""
+    if x is None or isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        return int(x.ctypes.data)
     return int(x.data_ptr())
 
 
@@ -136,6 +148,15 @@ def vitfe_embed(h, pixels, pixel_bytes, items, n_items, max_items, rows, out, st
     _check("vitfe_embed", load().vitfe_embed(h, _ptr(pixels), int(pixel_bytes), _ptr(items), _ptr(n_items),
                                              int(max_items), int(rows), _ptr(out), _ptr(status),
                                              _stream(stream)))
+
+
+def vitfe_embed_rope_host(h, pixels, pixel_bytes, items, n_items, out, head_dim, theta, cos, sin, status=None,
+                          chunks=16) -> None:
+    """Host buffers (numpy arrays, torch CPU tensors or int addresses)."""
+    _check("vitfe_embed_rope_host",
+           load().vitfe_embed_rope_host(h, _hptr(pixels), int(pixel_bytes), _hptr(items), int(n_items), _hptr(out),
+                                        int(head_dim), float(theta), _hptr(cos), _hptr(sin), _hptr(status),
+                                        int(chunks)))
 
 
 def vitfe_embed_folded(h, pixels, pixel_bytes, items, n_items, max_items, rows, out, status=None,

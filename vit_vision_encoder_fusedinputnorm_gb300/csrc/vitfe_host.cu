@@ -4,6 +4,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "vitfe_internal.cuh"
 
@@ -34,8 +35,42 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 constexpr int64_t kMaxRows = 0x7fffffffLL - 1024;
 
+void free_pipe_buffers(vitfe::Ctx::HostPipe& p) {
+  for (int b = 0; b < 2; ++b) {
+    if (p.px[b]) cudaFree(p.px[b]);
+    if (p.out[b]) cudaFree(p.out[b]);
+    if (p.cos[b]) cudaFree(p.cos[b]);
+    if (p.sin[b]) cudaFree(p.sin[b]);
+    p.px[b] = nullptr;
+    p.out[b] = nullptr;
+    p.cos[b] = p.sin[b] = nullptr;
+  }
+  p.px_cap = 0;
+  p.rows_cap = 0;
+  p.hd_cap = 0;
+}
+
+void free_pipe(vitfe::Ctx::HostPipe& p) {
+  free_pipe_buffers(p);
+  for (int b = 0; b < 2; ++b) {
+    if (p.items[b]) cudaFree(p.items[b]);
+    if (p.n[b]) cudaFree(p.n[b]);
+    if (p.status[b]) cudaFree(p.status[b]);
+    if (p.up[b]) cudaEventDestroy(p.up[b]);
+    if (p.done[b]) cudaEventDestroy(p.done[b]);
+    if (p.down[b]) cudaEventDestroy(p.down[b]);
+  }
+  if (p.h_items) cudaFreeHost(p.h_items);
+  if (p.h_small) cudaFreeHost(p.h_small);
+  if (p.h2d) cudaStreamDestroy(p.h2d);
+  if (p.comp) cudaStreamDestroy(p.comp);
+  if (p.d2h) cudaStreamDestroy(p.d2h);
+  p = vitfe::Ctx::HostPipe();
+}
+
 void free_ctx(vitfe_ctx* h) {
   if (!h) return;
+  free_pipe(h->c.pipe);
   if (h->c.w_tile) cudaFree(h->c.w_tile);
   if (h->c.w_tile_f) cudaFree(h->c.w_tile_f);
   if (h->c.bias) cudaFree(h->c.bias);
@@ -53,6 +88,57 @@ vitfe_status check_common(vitfe_t h, const vitfe_item* items, const int32_t* n_i
 }
 
 vitfe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? VITFE_OK : VITFE_ECUDA; }
+
+}  // namespace
+
+namespace {
+
+vitfe_status pipe_ready(vitfe::Ctx& c, size_t px_bytes, int64_t rows, int head_dim) {
+  auto& p = c.pipe;
+  if (!p.ready) {
+    bool ok = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p.comp, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) == cudaSuccess;
+    for (int b = 0; ok && b < 2; ++b)
+      ok = cudaEventCreateWithFlags(&p.up[b], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&p.done[b], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&p.down[b], cudaEventDisableTiming) == cudaSuccess &&
+           cudaMalloc(&p.items[b], sizeof(vitfe_item) * VITFE_MAX_ITEMS) == cudaSuccess &&
+           cudaMalloc(&p.n[b], sizeof(int32_t)) == cudaSuccess &&
+           cudaMalloc(&p.status[b], 2 * sizeof(int32_t)) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      free_pipe(p);
+      return VITFE_ENOMEM;
+    }
+    p.ready = true;
+  }
+  if (px_bytes > p.px_cap || rows > p.rows_cap || head_dim > p.hd_cap) {
+    // grow: nothing of this handle's pipeline may still be in flight
+    if (cudaStreamSynchronize(p.h2d) != cudaSuccess || cudaStreamSynchronize(p.comp) != cudaSuccess ||
+        cudaStreamSynchronize(p.d2h) != cudaSuccess)
+      return VITFE_ECUDA;
+    const size_t pxc = px_bytes > p.px_cap ? px_bytes : p.px_cap;
+    const int64_t rc = rows > p.rows_cap ? rows : p.rows_cap;
+    const int hc = head_dim > p.hd_cap ? head_dim : p.hd_cap;
+    free_pipe_buffers(p);
+    bool ok = true;
+    for (int b = 0; ok && b < 2; ++b)
+      ok = cudaMalloc(&p.px[b], pxc > 16 ? pxc : 16) == cudaSuccess &&
+           cudaMalloc(&p.out[b], (size_t)(rc > 1 ? rc : 1) * c.N * sizeof(__nv_bfloat16)) == cudaSuccess &&
+           cudaMalloc(&p.cos[b], (size_t)(rc > 1 ? rc : 1) * (hc / 2) * sizeof(float)) == cudaSuccess &&
+           cudaMalloc(&p.sin[b], (size_t)(rc > 1 ? rc : 1) * (hc / 2) * sizeof(float)) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      free_pipe_buffers(p);
+      return VITFE_ENOMEM;
+    }
+    p.px_cap = pxc;
+    p.rows_cap = rc;
+    p.hd_cap = hc;
+  }
+  return VITFE_OK;
+}
 
 }  // namespace
 
@@ -202,6 +288,159 @@ vitfe_status vitfe_embed_folded(vitfe_t h, const uint8_t* pixels, int64_t pixel_
   if (!h->c.embed_ok || h->c.w_tile_f == nullptr) return VITFE_EUNSUPPORTED;
   return from_cuda(vitfe::launch_embed(h->c, pixels, pixel_bytes, items, n_items, max_items, rows, out, status,
                                        stream, nullptr, 0, nullptr, nullptr, true));
+}
+
+// ---------------------------------------------------------------------------
+// Host-buffer pipeline: the items are cut into `chunks` runs of consecutive items with
+// about equal rows.  Chunk c uses device staging set c % 2: its pixels and descriptors go
+// up on one stream, the fused embed + RoPE launch runs on a second, the results come down
+// on a third, so chunk c's upload and launch overlap chunk c - 1's download.
+// ---------------------------------------------------------------------------
+
+vitfe_status vitfe_embed_rope_host(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes, const vitfe_item* items,
+                                   int32_t n_items, void* out, int head_dim, float theta, float* cos, float* sin,
+                                   int32_t* status, int32_t chunks) {
+  if (h == nullptr || n_items < 0 || n_items > VITFE_MAX_HOST_ITEMS || (n_items > 0 && items == nullptr))
+    return VITFE_EINVAL;
+  if (pixel_bytes < 0 || (pixel_bytes > 0 && pixels == nullptr) || chunks < 1) return VITFE_EINVAL;
+  if (head_dim < 8 || head_dim > VITFE_ROPE_MAX_HEAD_DIM || (head_dim % 8) != 0) return VITFE_EINVAL;
+  if (!std::isfinite(theta) || !(theta > 0.0f)) return VITFE_EINVAL;
+  vitfe::Ctx& c = h->c;
+  if (!c.embed_ok) return VITFE_EUNSUPPORTED;
+  // host-side validation: every item's pixels lie inside the host buffer
+  std::vector<int64_t> row0((size_t)n_items + 1, 0), pend((size_t)n_items, 0);
+  for (int i = 0; i < n_items; ++i) {
+    const vitfe_item& it = items[i];
+    if (it.t < 0 || it.h < 0 || it.w < 0 || it.frames < 1 || it.pixel_offset < 0 || (it.pixel_offset & 15))
+      return VITFE_EINVAL;
+    const int64_t r = (int64_t)it.t * it.h * it.w;
+    const int64_t bytes = (int64_t)it.frames * it.h * c.P * it.w * c.P * 3;
+    if (it.pixel_offset + bytes > pixel_bytes) return VITFE_EINVAL;
+    row0[i + 1] = row0[i] + r;
+    pend[i] = it.pixel_offset + bytes;
+    if (row0[i + 1] > kMaxRows) return VITFE_EINVAL;
+  }
+  const int64_t rows = row0[n_items];
+  if (rows > 0 && (out == nullptr || cos == nullptr || sin == nullptr)) return VITFE_EINVAL;
+  if (status != nullptr) {
+    status[0] = 0;
+    status[1] = -1;
+  }
+  if (n_items == 0) return VITFE_OK;
+  // chunk boundaries: runs of consecutive items with about rows / chunks rows, at most
+  // VITFE_MAX_ITEMS items each
+  std::vector<int> cut{0};
+  for (int i = 1; i < n_items; ++i) {
+    const int64_t target = rows * (int64_t)cut.size() / chunks;
+    if (row0[i] >= target || i - cut.back() >= VITFE_MAX_ITEMS) cut.push_back(i);
+  }
+  cut.push_back(n_items);
+  const int nch = (int)cut.size() - 1;
+  size_t px_max = 0;
+  int64_t rows_max = 0;
+  std::vector<int64_t> base((size_t)nch), span((size_t)nch);
+  for (int k = 0; k < nch; ++k) {
+    int64_t lo = items[cut[k]].pixel_offset, hi = lo;
+    for (int i = cut[k]; i < cut[k + 1]; ++i) {
+      lo = items[i].pixel_offset < lo ? items[i].pixel_offset : lo;
+      hi = pend[i] > hi ? pend[i] : hi;
+    }
+    base[k] = lo;
+    span[k] = (hi - lo + 15) / 16 * 16;
+    if (lo + span[k] > pixel_bytes) span[k] = pixel_bytes - lo;   // the last bytes of the buffer
+    px_max = (size_t)span[k] > px_max ? (size_t)span[k] : px_max;
+    const int64_t r = row0[cut[k + 1]] - row0[cut[k]];
+    rows_max = r > rows_max ? r : rows_max;
+  }
+  vitfe_status st = pipe_ready(c, px_max, rows_max, head_dim);
+  if (st != VITFE_OK) return st;
+  auto& p = c.pipe;
+  if ((size_t)n_items > p.h_items_cap) {
+    if (p.h_items) cudaFreeHost(p.h_items);
+    p.h_items = nullptr;
+    p.h_items_cap = 0;
+    if (cudaHostAlloc(reinterpret_cast<void**>(&p.h_items), sizeof(vitfe_item) * (size_t)n_items,
+                      cudaHostAllocDefault) != cudaSuccess) {
+      cudaGetLastError();
+      return VITFE_ENOMEM;
+    }
+    p.h_items_cap = (size_t)n_items;
+  }
+  if ((size_t)(3 * nch) > p.h_small_cap) {
+    if (p.h_small) cudaFreeHost(p.h_small);
+    p.h_small = nullptr;
+    p.h_small_cap = 0;
+    if (cudaHostAlloc(reinterpret_cast<void**>(&p.h_small), sizeof(int32_t) * 3 * (size_t)nch,
+                      cudaHostAllocDefault) != cudaSuccess) {
+      cudaGetLastError();
+      return VITFE_ENOMEM;
+    }
+    p.h_small_cap = 3 * (size_t)nch;
+  }
+  const float* tab = nullptr;
+  if (vitfe::rope_table_for(c, head_dim, theta, p.comp, &tab) != cudaSuccess) return VITFE_ECUDA;
+  // per-chunk descriptors (offsets relative to the chunk's pixel base) and statuses, kept
+  // until the pipeline drains
+  vitfe_item* chunk_items = p.h_items;
+  int32_t* counts = p.h_small;
+  int32_t* stat = p.h_small + nch;
+  for (int k = 0; k < 2 * nch; ++k) stat[k] = 0;
+  const int hh = head_dim / 2;
+  cudaError_t e = cudaSuccess;
+  for (int k = 0; k < nch && e == cudaSuccess; ++k) {
+    const int b = k & 1;
+    const int i0 = cut[k], ni = cut[k + 1] - i0;
+    const int64_t r0 = row0[i0], nr = row0[cut[k + 1]] - r0;
+    for (int i = 0; i < ni; ++i) {
+      chunk_items[(size_t)(i0 + i)] = items[i0 + i];
+      chunk_items[(size_t)(i0 + i)].pixel_offset -= base[k];
+    }
+    counts[(size_t)k] = ni;
+    // upload, once this staging set's previous download has finished
+    e = cudaStreamWaitEvent(p.h2d, p.down[b], 0);
+    if (e == cudaSuccess && span[k] > 0)
+      e = cudaMemcpyAsync(p.px[b], pixels + base[k], (size_t)span[k], cudaMemcpyHostToDevice, p.h2d);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(p.items[b], chunk_items + i0, sizeof(vitfe_item) * (size_t)ni,
+                          cudaMemcpyHostToDevice, p.h2d);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(p.n[b], counts + k, sizeof(int32_t), cudaMemcpyHostToDevice, p.h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(p.up[b], p.h2d);
+    // the fused launch
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p.comp, p.up[b], 0);
+    if (e == cudaSuccess)
+      e = vitfe::launch_embed(c, p.px[b], span[k], p.items[b], p.n[b], VITFE_MAX_ITEMS, nr, p.out[b], p.status[b],
+                              p.comp, tab, head_dim / 4, p.cos[b], p.sin[b]);
+    if (e == cudaSuccess) e = cudaEventRecord(p.done[b], p.comp);
+    // download
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p.d2h, p.done[b], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<__nv_bfloat16*>(out) + (size_t)r0 * c.N, p.out[b],
+                          (size_t)nr * c.N * sizeof(__nv_bfloat16), cudaMemcpyDeviceToHost, p.d2h);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(cos + (size_t)r0 * hh, p.cos[b], (size_t)nr * hh * sizeof(float), cudaMemcpyDeviceToHost,
+                          p.d2h);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(sin + (size_t)r0 * hh, p.sin[b], (size_t)nr * hh * sizeof(float), cudaMemcpyDeviceToHost,
+                          p.d2h);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(stat + 2 * k, p.status[b], 2 * sizeof(int32_t), cudaMemcpyDeviceToHost, p.d2h);
+    if (e == cudaSuccess) e = cudaEventRecord(p.down[b], p.d2h);
+  }
+  // drain every stream of the pipeline (also after an error: staging may not be reused early)
+  const cudaError_t e1 = cudaStreamSynchronize(p.h2d);
+  const cudaError_t e2 = cudaStreamSynchronize(p.comp);
+  const cudaError_t e3 = cudaStreamSynchronize(p.d2h);
+  if (e != cudaSuccess || e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) return VITFE_ECUDA;
+  if (status != nullptr) {
+    for (int k = 0; k < nch; ++k)
+      if (stat[2 * (size_t)k] != 0) {
+        status[0] = stat[2 * (size_t)k];
+        status[1] = stat[2 * (size_t)k + 1] >= 0 ? stat[2 * (size_t)k + 1] + cut[k] : -1;
+        break;
+      }
+  }
+  return VITFE_OK;
 }
 
 vitfe_status vitfe_embed_rope(vitfe_t h, const uint8_t* pixels, int64_t pixel_bytes, const vitfe_item* items,

@@ -34,8 +34,6 @@ struct Ctx {
   __nv_bfloat16* w_tile_f = nullptr;  // folded-still weight images (one slice: sum of the T slices)
   size_t w_tile_f_bytes = 0;
   float* bias = nullptr;           // [N] fp32 (zeros when no bias)
-  // RoPE axis tables (the cos/sin cache), one slot per (head_dim, theta) seen, each
-  // [2][VITFE_ROPE_MAX_SIDE][head_dim/4] fp32 covering every position, built on first use
   static constexpr int kRopeSlots = 4;
   // RoPE axis tables: kRopeSlots cached tables, each keyed by (head_dim, theta) for the
   // handle's lifetime (a slot is never given to another key, so a captured graph that
@@ -56,6 +54,27 @@ struct Ctx {
   size_t embed_smem = 0;           // dynamic shared memory of the embed kernel
   bool embed_ok = false;           // embed kernel supports this shape
   uint64_t wait_limit_ns = 1000000000ull;
+  // host-buffer pipeline of vitfe_embed_rope_host: created on first use, grown on demand
+  struct HostPipe {
+    bool ready = false;
+    cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+    cudaEvent_t up[2] = {nullptr, nullptr}, done[2] = {nullptr, nullptr}, down[2] = {nullptr, nullptr};
+    uint8_t* px[2] = {nullptr, nullptr};
+    size_t px_cap = 0;
+    vitfe_item* items[2] = {nullptr, nullptr};   // VITFE_MAX_ITEMS each
+    int32_t* n[2] = {nullptr, nullptr};
+    int32_t* status[2] = {nullptr, nullptr};
+    __nv_bfloat16* out[2] = {nullptr, nullptr};
+    float* cos[2] = {nullptr, nullptr};
+    float* sin[2] = {nullptr, nullptr};
+    int64_t rows_cap = 0;
+    int hd_cap = 0;
+    // page-locked host staging of the per-run descriptors, counts and status words: a copy
+    // from or to pageable memory would block the host and serialise the pipeline
+    vitfe_item* h_items = nullptr;
+    int32_t* h_small = nullptr;     // [runs] counts, then [runs][2] status words
+    size_t h_items_cap = 0, h_small_cap = 0;
+  } pipe;
 };
 
 constexpr int kMaxItems = VITFE_MAX_ITEMS;

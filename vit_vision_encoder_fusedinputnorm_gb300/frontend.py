@@ -98,6 +98,22 @@ class FrontEnd:
                                    status, self._stream(stream))
         return out
 
+    def embed_rope_host(self, item_list, head_dim: int, theta: float, chunks: int = 16, pinned: bool = True):
+        """Host in, host out, copies overlapped (vitfe_embed_rope_host): (out, cos, sin, status)
+        as torch CPU tensors (page-locked when ``pinned``)."""
+        torch = self.torch
+        items, buf, rows = B.pack_items(item_list, self.patch, self.tpatch)
+        px = torch.from_numpy(buf)
+        if pinned:
+            px = px.pin_memory()
+        it = torch.from_numpy(np.ascontiguousarray(items).view(np.uint8))
+        out = torch.empty((rows, self.hidden), dtype=torch.bfloat16, pin_memory=pinned)
+        cos = torch.empty((rows, head_dim // 2), dtype=torch.float32, pin_memory=pinned)
+        sin = torch.empty((rows, head_dim // 2), dtype=torch.float32, pin_memory=pinned)
+        st = torch.zeros(2, dtype=torch.int32)
+        B.vitfe_embed_rope_host(self.h, px, px.numel(), it, len(items), out, head_dim, theta, cos, sin, st, chunks)
+        return out, cos, sin, st
+
     def embed_folded(self, b: Batch, rows: Optional[int] = None, out=None, status=None, stream=None):
         """The folded-still variant of embed (an approximation; see vitfe_embed_folded)."""
         torch = self.torch
