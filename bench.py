@@ -147,6 +147,23 @@ def cpu_baseline(budget_s: float = 12.0):
                       f"(normalise, patchify, BLAS GEMM), {t_total:.1f} s"}
 
 
+def world_max(x: float, world: int, device) -> float:
+    """The slowest replica's figure: max over the ranks of the process group."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(rows_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job patches/s: every rank embeds its own copy of the workload (replicas, weak
+    scaling), so the job processes world * rows per step in the slowest rank's time."""
+    return world * rows_per_rank / (ms_per_step / 1e3)
+
+
 def run_reference(args, rank, world):
     """The oracle timed as the reference arm: each step a strip of one image, sized so
     the whole run stays within about two minutes."""
@@ -306,14 +323,10 @@ def main():
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
-    total_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = world_max(t0.elapsed_time(t1), world, dev)
     ms_step = total_ms / args.steps
     embed_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    value = world * rows / (ms_step / 1e3)
+    value = replica_value(rows, world, ms_step)
 
     # end to end through the host-buffer entry point (vitfe_embed_rope_host): page-locked
     # pixels and descriptors in, embeddings and cos/sin out, the copies overlapped with the
@@ -340,11 +353,7 @@ def main():
     t_e2e = time.perf_counter()
     for _ in range(args.e2e_steps):
         e2e_step()
-    e2e_ms = (time.perf_counter() - t_e2e) * 1e3 / args.e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = world_max((time.perf_counter() - t_e2e) * 1e3 / args.e2e_steps, world, dev)
 
     def timed(fn, n=8, skip=3):
         ts = []
