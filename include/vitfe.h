@@ -29,6 +29,11 @@
  *    (int32[2] = {code, item index or -1}); every device call overwrites it
  *    ({0, -1} on success).  Rows of an item found invalid on the device are
  *    written as the pad value; nothing is read out of range and nothing traps.
+ *  - Every wait inside a kernel is bounded (1 s, or VITFE_WAIT_LIMIT_MS at
+ *    vitfe_create); on expiry the launch drains its asynchronous work, frees
+ *    what it holds and reports VITFE_EDEVICE_TIMEOUT (outputs invalid), and the
+ *    context stays usable.  VITFE_TEST_STALL_W_LOADS=1 at vitfe_create makes
+ *    the embed kernel load no weights, to exercise that path in tests.
  *  - Bucket padding: rows at or past sum(t*h*w) up to `rows` are written as
  *    embedding 0, cos 1, sin 0, position id -1, flatten_patches 0.
  *  - Pixel reads: the library reads whole aligned 4-byte words that overlap

@@ -595,3 +595,31 @@ def test_embed_rope_host_reports_errors():
     assert st.tolist() == [4, 2]
     assert np.all(out[rows_bad - 6 * 3:] == 0)
     fe.close()
+
+
+def test_bounded_wait_runs_out_and_reports_timeout(monkeypatch):
+    # failure detection without a fault: a handle whose weight producer issues no loads
+    # (test hook) leaves the MMA's wait unsatisfied; after the short limit every role leaves,
+    # the launch reports VITFE_EDEVICE_TIMEOUT, and the context keeps working
+    wl = synth.small_workload(61, [(1, 4, 6, 1), (2, 2, 4, 4)], patch=14, hidden=256, head_dim=80)
+    monkeypatch.setenv("VITFE_WAIT_LIMIT_MS", "200")
+    monkeypatch.setenv("VITFE_TEST_STALL_W_LOADS", "1")
+    stalled = _fe(wl)
+    monkeypatch.delenv("VITFE_TEST_STALL_W_LOADS")
+    monkeypatch.delenv("VITFE_WAIT_LIMIT_MS")
+    b = stalled.upload(wl.items)
+    st = stalled.status_tensor()
+    stalled.embed(b, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [6, -1]
+    stalled.close()
+    # the same process and context: a normal handle still computes correct embeddings
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    st = fe.status_tensor()
+    out = fe.embed(b, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, -1]
+    rel, mx = U.embed_errors(U.bits_to_f64(U.tensor_bits(out)), oracle.embed_workload(wl), U.item_starts(wl.items))
+    assert rel <= U.EMBED_REL_FROB and mx <= U.EMBED_MAX_ABS
+    fe.close()

@@ -64,6 +64,7 @@ struct EmbedArgs {
   int tmem_cols;
   int num_tiles;   // 256-row pair tiles
   uint64_t limit_ns;
+  int stall_w_loads;       // test hook: the weight producer issues nothing
   // 2D-RoPE rows written by the same launch (null: embeddings only)
   const float* rope_tab;   // the handle's axis table: cos [p * nf + i], sin after VITFE_ROPE_MAX_SIDE rows
   float* rope_cos;
@@ -491,7 +492,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       cur = nxt;
     }
   } else if (warp == kTmaWarp) {
-    if (lane == 0) {
+    // (with the failure-detection test hook set, no weight tile is ever loaded: the MMA's
+    // bounded wait runs out, every role leaves on the abort flag or its own limit)
+    if (lane == 0 && !args.stall_w_loads) {
       // W tiles in consumption order: one stage per step (a step = one 64-feature K block
       // of one temporal slice)
       uint32_t nb = 0, stage = 0, bphase = 0;
@@ -828,6 +831,7 @@ cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_byte
   while (a.tmem_cols < 2 * c.bn) a.tmem_cols <<= 1;
   a.num_tiles = (int)((rows + kPairRows - 1) / kPairRows);
   a.limit_ns = c.wait_limit_ns;
+  a.stall_w_loads = c.test_stall_w_loads ? 1 : 0;
   a.rope_tab = rope_tab;
   a.rope_cos = rope_cos;
   a.rope_sin = rope_sin;

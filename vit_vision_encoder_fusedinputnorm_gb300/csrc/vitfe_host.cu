@@ -197,6 +197,7 @@ vitfe_status vitfe_create(vitfe_t* out, const float mean[3], const float std_[3]
     const long ms = std::strtol(env, nullptr, 10);
     if (ms > 0) c.wait_limit_ns = (uint64_t)ms * 1000000ull;
   }
+  if (const char* env = std::getenv("VITFE_TEST_STALL_W_LOADS")) c.test_stall_w_loads = env[0] == '1';
 
   if (cudaMalloc(&c.bias, (size_t)c.N * sizeof(float)) != cudaSuccess ||
       cudaMalloc(&c.rope_tab, (size_t)(vitfe::Ctx::kRopeSlots + 1) * 2 * VITFE_ROPE_MAX_SIDE * (VITFE_ROPE_MAX_HEAD_DIM / 4) *

@@ -54,6 +54,10 @@ struct Ctx {
   size_t embed_smem = 0;           // dynamic shared memory of the embed kernel
   bool embed_ok = false;           // embed kernel supports this shape
   uint64_t wait_limit_ns = 1000000000ull;
+  // failure-detection test hook (VITFE_TEST_STALL_W_LOADS=1 at create): the embed kernel's
+  // weight producer issues no loads, so the MMA's bounded wait runs out and the launch
+  // reports VITFE_EDEVICE_TIMEOUT
+  bool test_stall_w_loads = false;
   // host-buffer pipeline of vitfe_embed_rope_host: created on first use, grown on demand
   struct HostPipe {
     bool ready = false;
