@@ -390,6 +390,19 @@ def main():
                                                      batch.n_items, batch.capacity, rows, flat, None, stream))
     np_bytes = batch.pixel_bytes + rows * K * 2
 
+    # the patch-16 bucket workload (Qwen3-VL-like: K 1536, N 1152): one 65,536-row bucket of
+    # the varied stills, embedded with its own handle (a parity case; timed here for reference)
+    wl4 = synth.make_workload(4)
+    fe4 = FrontEnd.from_workload(wl4, device=f"cuda:{local}")
+    b4 = fe4.upload([wl4.items[i] for i in wl4.buckets[0]])
+    out4 = torch.empty((b4.live_rows, wl4.hidden), dtype=torch.bfloat16, device=dev)
+    p16_ms = timed(lambda: B.vitfe_embed(fe4.h, b4.pixels, b4.pixel_bytes, b4.items, b4.n_items, b4.capacity,
+                                         b4.live_rows, out4, None, stream))
+    p16_tflops = 2.0 * b4.live_rows * wl4.K * wl4.hidden / (p16_ms / 1e3) / 1e12
+    p16_rows = b4.live_rows
+    del out4, b4
+    fe4.close()
+
     # RoPE applied to Q and K (16 + 16 heads of 80, views into a packed [rows][Q | K | V]
     # buffer), from the step's cos/sin tables: HBM bound, in place
     heads = N // wl.head_dim
@@ -420,6 +433,8 @@ def main():
                      "kernel": "embed_kernel<14>", "flops_per_launch": flops,
                      "kernel_ms": embed_ms},
         "side_paths": {"unfused_embed_then_rope_ms": unfused_ms,
+                       "patch16_bucket_embed": {"rows": p16_rows, "ms": p16_ms, "tflops": p16_tflops,
+                                                "frac_of_peak": p16_tflops / float(pk["bf16_tflops"])},
                        "folded_still_variant": {"ms": folded_ms, "patches_per_s": world * rows / (folded_ms / 1e3),
                                                 "note": "approximation (W slices summed, rounded once to bf16); "
                                                         "K 588 for stills; not the method's exact result"},
