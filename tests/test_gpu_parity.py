@@ -217,12 +217,20 @@ def test_full_workload_embed(cfg):
 
 
 def test_throughput_workload_sampled():
-    # 64 x 1344^2 stills, in the launch configuration the benchmark times; sampled rows:
-    # both sides of every 128-row tile boundary plus random rows.
+    # 64 x 1344^2 stills, through the call and launch configuration the benchmark times
+    # (vitfe_embed_rope); sampled embedding rows: both sides of every 128-row CTA tile
+    # boundary plus random rows; the RoPE rows in full.
     wl = synth.make_workload(2)
     fe = _fe(wl)
     b = fe.upload(wl.items)
-    out = fe.embed(b)
+    st = fe.status_tensor()
+    out, cos, sin = fe.embed_rope(b, wl.head_dim, wl.theta, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, -1]
+    rc, rs = oracle.rope_workload(wl)
+    assert np.max(np.abs(cos.cpu().numpy() - rc)) <= U.ROPE_MAX_ABS
+    assert np.max(np.abs(sin.cpu().numpy() - rs)) <= U.ROPE_MAX_ABS
+    del cos, sin
     rows = b.live_rows
     rng = np.random.default_rng(0)
     bnd = np.arange(128, rows, 128)
