@@ -631,3 +631,46 @@ def test_bounded_wait_runs_out_and_reports_timeout(monkeypatch):
     rel, mx = U.embed_errors(U.bits_to_f64(U.tensor_bits(out)), oracle.embed_workload(wl), U.item_starts(wl.items))
     assert rel <= U.EMBED_REL_FROB and mx <= U.EMBED_MAX_ABS
     fe.close()
+
+
+SHAPES = {
+    # (patch, tpatch, merge, grids (t, h, w, frames))
+    "p14_t1_m2": (14, 1, 2, [(1, 4, 6, 1), (3, 2, 4, 3), (1, 6, 2, 1)]),     # generic normalise kernel
+    "p16_t1_m2": (16, 1, 2, [(1, 4, 6, 1), (2, 2, 4, 2)]),                   # <16, 1> normalise kernel
+    "p14_t2_m1": (14, 2, 1, [(1, 3, 5, 1), (2, 1, 3, 4), (1, 7, 1, 1)]),     # no merge grouping
+    "p14_t2_m4": (14, 2, 4, [(1, 4, 8, 1), (2, 4, 4, 4)]),                   # 4 x 4 merge units
+    "p8_t2_m2": (8, 2, 2, [(1, 4, 6, 1), (2, 2, 4, 4)]),                     # no embed kernel for patch 8
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHAPES))
+def test_other_patch_temporal_and_merge_shapes(name):
+    from vit_vision_encoder_fusedinputnorm_gb300 import binding as B
+    P, T, M, grids = SHAPES[name]
+    wl = synth.small_workload(71, grids, patch=P, tpatch=T, merge=M, hidden=256, pixels="uniform")
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    rows = b.live_rows + 19
+    flat = fe.normalize_patchify(b, rows=rows)
+    got = U.tensor_bits(flat)
+    ref = U.f64_to_bf16_bits(oracle.normalize_patchify_workload(wl, bucket_rows=rows))
+    assert int(U.ulp_distance(got, ref).max()) <= U.NORM_MAX_ULP
+    assert np.array_equal(fe.pos_ids(b, rows=rows).cpu().numpy(), oracle.pos_ids_workload(wl, bucket_rows=rows))
+    cos, sin = fe.rope(b, wl.head_dim, wl.theta, rows=rows)
+    rc, rs = oracle.rope_workload(wl, bucket_rows=rows)
+    assert np.max(np.abs(cos.cpu().numpy() - rc)) <= U.ROPE_MAX_ABS
+    assert np.max(np.abs(sin.cpu().numpy() - rs)) <= U.ROPE_MAX_ABS
+    if P in (14, 16):
+        st = fe.status_tensor()
+        out = fe.embed(b, rows=rows, status=st)
+        torch.cuda.synchronize()
+        assert st.cpu().tolist() == [0, -1]
+        e = U.bits_to_f64(U.tensor_bits(out))
+        rel, mx = U.embed_errors(e, oracle.embed_workload(wl, bucket_rows=rows), U.item_starts(wl.items))
+        assert rel <= U.EMBED_REL_FROB and mx <= U.EMBED_MAX_ABS, (rel, mx)
+        assert np.all(U.tensor_bits(out)[b.live_rows:] == 0)
+    else:
+        with pytest.raises(B.VitfeError) as err:
+            fe.embed(b, rows=rows)
+        assert err.value.code == 7
+    fe.close()
