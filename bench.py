@@ -400,8 +400,39 @@ def main():
                                          b4.live_rows, out4, None, stream))
     p16_tflops = 2.0 * b4.live_rows * wl4.K * wl4.hidden / (p16_ms / 1e3) / 1e12
     p16_rows = b4.live_rows
-    del out4, b4
+    # ... and as the serving path runs it: one captured graph of the fused call over the fixed
+    # 65,536-row bucket (pad rows masked), replayed
+    R4 = wl4.bucket_rows
+    gout = torch.empty((R4, wl4.hidden), dtype=torch.bfloat16, device=dev)
+    gcos = torch.empty((R4, wl4.head_dim // 2), dtype=torch.float32, device=dev)
+    gsin = torch.empty_like(gcos)
+
+    def fused4():
+        B.vitfe_embed_rope(fe4.h, b4.pixels, b4.pixel_bytes, b4.items, b4.n_items, b4.capacity, R4, gout,
+                           wl4.head_dim, wl4.theta, gcos, gsin, None, stream)
+
+    with torch.cuda.stream(stream):
+        fused4()                       # builds the RoPE table outside the capture
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        fused4()
+    p16_graph_ms = timed(graph.replay)
+    del out4, b4, gout, gcos, gsin, graph
     fe4.close()
+
+    # the small, launch-bound workloads: one 224x224 image (256 patches) and 8 mixed images
+    # (18,048 patches), fused call latency
+    small = {}
+    for cfg_small in (0, 1):
+        wls = synth.make_workload(cfg_small)
+        fes = FrontEnd.from_workload(wls, device=f"cuda:{local}")
+        bs = fes.upload(wls.items)
+        o_s, c_s, s_s = fes.embed_rope(bs, wls.head_dim, wls.theta)
+        small[cfg_small] = (bs.live_rows, timed(lambda: B.vitfe_embed_rope(
+            fes.h, bs.pixels, bs.pixel_bytes, bs.items, bs.n_items, bs.capacity, bs.live_rows, o_s, wls.head_dim,
+            wls.theta, c_s, s_s, None, stream)))
+        fes.close()
 
     # RoPE applied to Q and K (16 + 16 heads of 80, views into a packed [rows][Q | K | V]
     # buffer), from the step's cos/sin tables: HBM bound, in place
@@ -434,7 +465,11 @@ def main():
                      "kernel_ms": embed_ms},
         "side_paths": {"unfused_embed_then_rope_ms": unfused_ms,
                        "patch16_bucket_embed": {"rows": p16_rows, "ms": p16_ms, "tflops": p16_tflops,
-                                                "frac_of_peak": p16_tflops / float(pk["bf16_tflops"])},
+                                                "frac_of_peak": p16_tflops / float(pk["bf16_tflops"]),
+                                                "graph_replay_embed_rope_ms": p16_graph_ms,
+                                                "bucket_rows": R4},
+                       "small_workload_embed_rope_us": {"1 x 224x224 (256 patches)": small[0][1] * 1e3,
+                                                        "8 mixed images (18,048 patches)": small[1][1] * 1e3},
                        "folded_still_variant": {"ms": folded_ms, "patches_per_s": world * rows / (folded_ms / 1e3),
                                                 "note": "approximation (W slices summed, rounded once to bf16); "
                                                         "K 588 for stills; not the method's exact result"},

@@ -35,6 +35,8 @@ SMALL = {
     "mixed_p14": (14, 1280, [(2, 4, 6, 4), (1, 6, 8, 1), (3, 2, 4, 6), (1, 2, 2, 1)]),
     "video_p14": (14, 512, [(4, 8, 10, 8)]),
     "stills_p16": (16, 1152, [(1, 4, 4, 1), (1, 6, 10, 1), (2, 4, 2, 4)]),
+    # all stills, five N passes: resident tiles whose passes are spread over several CTA pairs
+    "allstill_p14_n1280": (14, 1280, [(1, 2, 2, 1), (1, 4, 6, 1), (1, 16, 16, 1)]),
 }
 
 

@@ -63,6 +63,9 @@ struct EmbedArgs {
   int bn, nstage, npass;
   int tmem_cols;
   int num_tiles;   // 256-row pair tiles
+  // work units: each pair tile's npass N passes in `split` groups of ppu passes (split > 1
+  // only when there are fewer tiles than CTA pairs); unit u = tile * split + group
+  int split, ppu, num_units;
   uint64_t limit_ns;
   int stall_w_loads;       // test hook: the weight producer issues nothing
   // 2D-RoPE rows written by the same launch (null: embeddings only)
@@ -467,15 +470,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int rofs = (int)rank * kTileM + row;
     uint32_t np = 0;
     bool ok = true;
-    int tile = cid;
-    RowSrc cur = tile < args.num_tiles ? row_src<P>(args, hs, tile * kPairRows + rofs) : RowSrc{nullptr, 0, 0};
+    int u = cid;
+    RowSrc cur = u < args.num_units ? row_src<P>(args, hs, (u / args.split) * kPairRows + rofs)
+                                    : RowSrc{nullptr, 0, 0};
     if (half == 0) prefetch_row<P>(cur, args.T);
-    for (; ok && tile < args.num_tiles; tile += ncl) {
+    for (; ok && u < args.num_units; u += ncl) {
+      const int tile = u / args.split;
+      const int npu = min(args.ppu, args.npass - (u - tile * args.split) * args.ppu);   // passes of the unit
       const int kind = tile_kind(tile * kPairRows, hs, args.T);
-      const int next = tile + ncl;
-      const RowSrc nxt = next < args.num_tiles ? row_src<P>(args, hs, next * kPairRows + rofs) : RowSrc{nullptr, 0, 0};
+      const int next = u + ncl;
+      const RowSrc nxt = next < args.num_units ? row_src<P>(args, hs, (next / args.split) * kPairRows + rofs)
+                                               : RowSrc{nullptr, 0, 0};
       if (kind != kPad) {
-        const int nprod = (kind == kResident) ? 1 : args.npass * args.T;
+        const int nprod = (kind == kResident) ? 1 : npu * args.T;
         for (int q = 0; ok && q < nprod; ++q) {
           const int s = (kind == kResident) ? 0 : (q % args.T);
           const uint8_t* base = cur.base0 ? cur.base0 + cur.fstride * s : nullptr;
@@ -499,7 +506,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // of one temporal slice)
       uint32_t nb = 0, stage = 0, bphase = 0;
       bool ok = true;
-      for (int tile = cid; ok && tile < args.num_tiles; tile += ncl) {
+      for (int u = cid; ok && u < args.num_units; u += ncl) {
+        const int tile = u / args.split;
+        const int p_lo = (u - tile * args.split) * args.ppu;
+        const int p_hi = min(args.npass, p_lo + args.ppu);
         const int kind = tile_kind(tile * kPairRows, hs, args.T);
         if (kind == kPad) continue;
         // folded still tiles: one slice of the folded weight per block
@@ -507,7 +517,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int Ts = fold ? 1 : args.T;
         const CUtensorMap* map = fold ? &tmap_wf : &tmap_w;
         const int nsteps = Ts * NBLK;
-        for (int p = 0; ok && p < args.npass; ++p) {
+        for (int p = p_lo; ok && p < p_hi; ++p) {
           // this CTA's images of pass p: (p, rank, slice, block), bnh/4 rows of 512 B each
           const int blk0 = (p * 2 + (int)rank) * Ts * NBLK;
           for (int st = 0; ok && st < nsteps; ++st) {
@@ -592,10 +602,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }                                                                                         \
   } while (0)
 
-      for (int tile = cid; ok && tile < args.num_tiles; tile += ncl) {
+      for (int u = cid; ok && u < args.num_units; u += ncl) {
+        const int tile = u / args.split;
+        const int p_lo = (u - tile * args.split) * args.ppu;
+        const int p_hi = min(args.npass, p_lo + args.ppu);
         const int kind = tile_kind(tile * kPairRows, hs, args.T);
         if (kind == kPad) continue;
-        for (int p = 0; ok && p < args.npass; ++p) {
+        for (int p = p_lo; ok && p < p_hi; ++p) {
           const uint32_t buf = na & 1u;
           if (!mbar_wait_warp<true>(smem_u32(&hs->acc_empty[buf]), ((na >> 1) & 1u) ^ 1u, abort_flag, args.limit_ns)) {
             ok = false;
@@ -611,7 +624,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < NBLK; ++jj) {
               const int j = blk_order<NBLK>(jj);
-              if (p == 0) VITFE_WAIT_A(j);
+              if (p == p_lo) VITFE_WAIT_A(j);   // the unit's first pass meets the fresh A
               const uint64_t ad = adesc0 + (uint64_t)(j * (kABlockBytes >> 4));
               for (int sl = 0; ok && sl < Ts; ++sl) {
                 VITFE_WAIT_B();
@@ -619,7 +632,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 VITFE_STEP(ad, ksteps_of<P>(j), j == 0 && sl == 0);
               }
               if (!ok) break;
-              if (p == args.npass - 1) {
+              if (p == p_hi - 1) {
                 if (elect_one()) umma_commit_pair(a_empty0 + 8u * j);
                 __syncwarp();
               }
@@ -665,7 +678,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const bool out32 = (reinterpret_cast<uintptr_t>(args.out) & 31u) == 0;
     uint32_t na = 0;
     bool ok = true;
-    for (int tile = cid; ok && tile < args.num_tiles; tile += ncl) {
+    for (int u = cid; ok && u < args.num_units; u += ncl) {
+      const int tile = u / args.split;
+      const int p_lo = (u - tile * args.split) * args.ppu;
+      const int p_hi = min(args.npass, p_lo + args.ppu);
       const int r0 = tile * kPairRows;
       const int kind = tile_kind(r0, hs, args.T);
       const int r = r0 + rloc;
@@ -683,19 +699,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const int rope_wbase = r0 + (int)rank * kTileM + q * 32;
       __nv_bfloat16* orow = args.out + (size_t)r * (size_t)args.N;
+      // this unit's columns; the unit holding pass 0 also writes the rows' RoPE
+      const bool rope_unit = args.rope_cos != nullptr && p_lo == 0;
       if (kind == kPad) {
         if (in_bucket) {
           const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-          for (int c = 0; c < args.N; c += 8) *reinterpret_cast<uint4*>(orow + c) = z;
+          const int c_hi = min(args.N, p_hi * args.bn);
+          for (int c = p_lo * args.bn; c < c_hi; c += 8) *reinterpret_cast<uint4*>(orow + c) = z;
         }
-        if (args.rope_cos != nullptr) rope_rows(args, rope_wbase, hp, wp, lane);
+        if (rope_unit) rope_rows(args, rope_wbase, hp, wp, lane);
         continue;
       }
       // the RoPE rows of this warp's 32 tile rows go out after the second pass's accumulator:
       // the producers are idle then (they fill the next tile's A during the first and last
       // passes) and the epilogue waits for the next accumulator anyway
-      const int rope_pass = args.npass > 1 ? 1 : 0;
-      for (int p = 0; p < args.npass; ++p) {
+      const int rope_pass = p_hi - p_lo > 1 ? p_lo + 1 : p_lo;
+      for (int p = p_lo; p < p_hi; ++p) {
         const uint32_t buf = na & 1u;
         // warp-uniform wait: tcgen05.ld below (and the RoPE rows' shuffles) need the whole warp
         if (!mbar_wait_warp<true>(smem_u32(&hs->acc_full[buf]), (na >> 1) & 1u, abort_flag, args.limit_ns, 64)) {
@@ -736,7 +755,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive_cluster(acc_empty_L + 8u * buf);
         ++na;
-        if (args.rope_cos != nullptr && p == rope_pass) rope_rows(args, rope_wbase, hp, wp, lane);
+        if (rope_unit && p == rope_pass) rope_rows(args, rope_wbase, hp, wp, lane);
       }
     }
   }
@@ -830,6 +849,17 @@ cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_byte
   a.tmem_cols = 32;
   while (a.tmem_cols < 2 * c.bn) a.tmem_cols <<= 1;
   a.num_tiles = (int)((rows + kPairRows - 1) / kPairRows);
+  // fewer tiles than CTA pairs: spread each tile's N passes over several pairs (each
+  // produces the tile's A itself), so a small batch is not one pair's five passes in a row
+  {
+    int split = 1;
+    if (a.num_tiles > 0 && a.num_tiles < c.max_clusters) split = c.max_clusters / a.num_tiles;
+    if (split > a.npass) split = a.npass;
+    if (split < 1) split = 1;
+    a.ppu = (a.npass + split - 1) / split;
+    a.split = (a.npass + a.ppu - 1) / a.ppu;
+    a.num_units = a.num_tiles * a.split;
+  }
   a.limit_ns = c.wait_limit_ns;
   a.stall_w_loads = c.test_stall_w_loads ? 1 : 0;
   a.rope_tab = rope_tab;
@@ -837,7 +867,7 @@ cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_byte
   a.rope_sin = rope_sin;
   a.rope_nf = rope_nf;
   a.folded = folded ? 1 : 0;
-  int pairs = a.num_tiles < c.max_clusters ? a.num_tiles : c.max_clusters;
+  int pairs = a.num_units < c.max_clusters ? a.num_units : c.max_clusters;
   if (pairs < 1) pairs = 1;
   const int grid = 2 * pairs;
   if (c.P == 14)
