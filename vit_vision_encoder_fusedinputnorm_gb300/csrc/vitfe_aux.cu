@@ -707,23 +707,29 @@ int grid_for(long long work, int per_cta, int cap) {
 }
 
 template <int P, int T>
+constexpr size_t np_p_stage_bytes() {
+  return (size_t)(kAuxThreads / 32) * (np_stage_rs(P, 3 * T * P * P / 2) + 3 * T * P * P / 2) * 4;
+}
+
+// Opt the specialised kernel of (P, T) into its stage size and record its resident CTAs per
+// SM in the handle (its persistent grid is SMs x that).
+template <int P, int T>
+cudaError_t np_p_configure(Ctx& c) {
+  const size_t stage_bytes = np_p_stage_bytes<P, T>();
+  cudaError_t e = cudaFuncSetAttribute(normalize_patchify_p_kernel<P, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)stage_bytes);
+  if (e != cudaSuccess) return e;
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, normalize_patchify_p_kernel<P, T>, kAuxThreads, stage_bytes);
+  if (e != cudaSuccess) return e;
+  c.np_per_sm = n > 0 ? n : 1;
+  return cudaSuccess;
+}
+
+template <int P, int T>
 cudaError_t launch_np_p(const Ctx& c, const NpArgs& a, cudaStream_t s) {
-  constexpr int KW = 3 * T * P * P / 2;
-  constexpr int RS = np_stage_rs(P, KW);
-  const size_t stage_bytes = (size_t)(kAuxThreads / 32) * (RS + KW) * 4;
-  static int per_sm = 0;     // resident CTAs per SM (same on every device of one kind), queried once
-  if (per_sm == 0) {
-    cudaError_t e = cudaFuncSetAttribute(normalize_patchify_p_kernel<P, T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stage_bytes);
-    if (e != cudaSuccess) return e;
-    int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, normalize_patchify_p_kernel<P, T>, kAuxThreads,
-                                                      stage_bytes);
-    if (e != cudaSuccess) return e;
-    per_sm = n > 0 ? n : 1;
-  }
-  const int grid = grid_for(a.rows, (kAuxThreads / 32) * kNpWarpRows, c.sm_count * per_sm);
-  normalize_patchify_p_kernel<P, T><<<grid, kAuxThreads, stage_bytes, s>>>(a);
+  const int grid = grid_for(a.rows, (kAuxThreads / 32) * kNpWarpRows, c.sm_count * c.np_per_sm);
+  normalize_patchify_p_kernel<P, T><<<grid, kAuxThreads, np_p_stage_bytes<P, T>(), s>>>(a);
   return cudaGetLastError();
 }
 
@@ -877,6 +883,13 @@ cudaError_t launch_rope(Ctx& c, const vitfe_item* items, const int32_t* n_items,
   rope_expand_kernel<<<grid, kAuxThreads, 0, s>>>(items, n_items, max_items, c.T, c.M, (int)rows, nf, tab, cos, sin,
                                                   status);
   return cudaGetLastError();
+}
+
+cudaError_t np_configure(Ctx& c) {
+  if (c.P == 14 && c.T == 2) return np_p_configure<14, 2>(c);
+  if (c.P == 16 && c.T == 2) return np_p_configure<16, 2>(c);
+  if (c.P == 16 && c.T == 1) return np_p_configure<16, 1>(c);
+  return cudaSuccess;
 }
 
 cudaError_t launch_normalize_patchify(const Ctx& c, const uint8_t* pixels, int64_t pixel_bytes,

@@ -209,6 +209,7 @@ vitfe_status vitfe_create(vitfe_t* out, const float mean[3], const float std_[3]
   }
   // the embed kernel's tile shape decides the weight layout
   cudaError_t e = vitfe::embed_configure(c);
+  if (e == cudaSuccess) e = vitfe::np_configure(c);
   if (e != cudaSuccess) {
     free_ctx(h);
     return VITFE_ECUDA;

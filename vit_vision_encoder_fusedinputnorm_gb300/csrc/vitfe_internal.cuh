@@ -58,6 +58,7 @@ struct Ctx {
   // weight producer issues no loads, so the MMA's bounded wait runs out and the launch
   // reports VITFE_EDEVICE_TIMEOUT
   bool test_stall_w_loads = false;
+  int np_per_sm = 1;               // resident CTAs per SM of the specialised normalise+patchify kernel
   // host-buffer pipeline of vitfe_embed_rope_host: created on first use, grown on demand
   struct HostPipe {
     bool ready = false;
@@ -532,6 +533,7 @@ cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_byte
                          const float* rope_tab = nullptr, int rope_nf = 0, float* rope_cos = nullptr,
                          float* rope_sin = nullptr, bool folded = false);
 cudaError_t embed_configure(Ctx& c);
+cudaError_t np_configure(Ctx& c);   // at create: the normalise+patchify kernel's smem and occupancy
 // The handle's cos/sin axis table of (head_dim, theta): found in its slots, or built there
 // (one launch on `s`) the first time.  Layout: cos at [p * nf + i], sin at
 // [VITFE_ROPE_MAX_SIDE * nf + p * nf + i], nf = head_dim / 4, p < VITFE_ROPE_MAX_SIDE.
