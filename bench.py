@@ -46,10 +46,16 @@ def peaks():
 
 
 def source_hash() -> str:
+    """Hash of the embed kernel's code (comments and whitespace stripped, so that editing a
+    comment does not disown the committed ncu traffic figure)."""
+    import re
     h = hashlib.sha256()
     for f in ["vitfe_embed.cu", "vitfe_internal.cuh"]:
-        with open(os.path.join(ROOT, "vit_vision_encoder_fusedinputnorm_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "vit_vision_encoder_fusedinputnorm_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

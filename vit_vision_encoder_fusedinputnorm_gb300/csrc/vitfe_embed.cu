@@ -15,10 +15,12 @@
 //               features each);
 //   warp 12     TMA producer of this CTA's half of each W tile: one box copies one
 //               shared-memory image of the pre-tiled weight (bn/8 rows of 512 bytes);
-//   warp 13     tensor-memory allocation (both CTAs); in the even CTA one thread issues
-//               the MMAs (fp32 accumulators double-buffered in tensor memory);
+//   warp 13     tensor-memory allocation (both CTAs); in the even CTA the whole warp runs
+//               the MMA issue loop and one elected lane issues (fp32 accumulators
+//               double-buffered in tensor memory);
 //   warps 8-11  epilogue, one warp per tensor-memory lane quarter: tcgen05.ld of the
-//               accumulator, + bias, bf16 RNE, 256-bit stores.
+//               accumulator, + bias, bf16 RNE, 256-bit stores; in a vitfe_embed_rope
+//               launch also the tile's 2D-RoPE rows.
 // Barriers that gather both CTAs (A ready, W tile ready, accumulator free) live in the
 // even CTA; the MMA's completion is multicast to both CTAs.
 //
@@ -28,6 +30,10 @@
 // while the tile loops over the N passes; for stills the temporal slices are equal,
 // so one resident slice feeds the MMAs of every slice ("resident" tiles).  Tiles
 // holding video rows re-produce A per (pass, slice) ("stream" tiles).
+//
+// The K blocks are consumed in the order the producer threads fill them (one block of each
+// producer range in turn).  The work unit is (pair tile, group of N passes): a batch with
+// fewer tiles than CTA pairs spreads each tile's passes over several pairs.
 //
 // Every mbarrier wait is bounded (global timer); on expiry the CTA drains its async
 // copies and MMAs, frees its tensor memory, writes VITFE_EDEVICE_TIMEOUT and exits.
