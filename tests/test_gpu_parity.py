@@ -130,6 +130,27 @@ def test_still_equals_duplicated_two_frame_item():
     fe.close()
 
 
+def test_last_round_pass_split_equals_unsplit():
+    # One tile more than CTA pairs: the last round's tile has its N passes spread over
+    # several pairs.  A bucket of whole rounds runs the same rows unsplit; every row's
+    # embedding must be bit-identical (all stills: the same resident summation order), and
+    # the split tile's rows match the oracle.
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    n = pairs + 1
+    wl = synth.small_workload(47, [(1, 16, 16, 1)] * n, patch=14, hidden=1280)
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    assert b.live_rows == 256 * n
+    a = U.tensor_bits(fe.embed(b, rows=b.live_rows))
+    u = U.tensor_bits(fe.embed(b, rows=2 * 256 * pairs)[: b.live_rows])
+    assert np.array_equal(a, u)
+    ref = oracle.embed_workload(wl, items=[n - 1])
+    g = U.bits_to_f64(a[-256:])
+    rel, mx = U.embed_errors(g, ref, [0, 256])
+    assert rel <= U.EMBED_REL_FROB and mx <= U.EMBED_MAX_ABS
+    fe.close()
+
+
 def test_deterministic_rerun():
     wl = synth.make_workload(1)
     fe = _fe(wl)

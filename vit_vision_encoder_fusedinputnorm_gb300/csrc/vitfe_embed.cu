@@ -32,8 +32,8 @@
 // holding video rows re-produce A per (pass, slice) ("stream" tiles).
 //
 // The K blocks are consumed in the order the producer threads fill them (one block of each
-// producer range in turn).  The work unit is (pair tile, group of N passes): a batch with
-// fewer tiles than CTA pairs spreads each tile's passes over several pairs.
+// producer range in turn).  The work unit is (pair tile, group of N passes): the tiles of
+// a last round with fewer tiles than CTA pairs have their passes spread over several pairs.
 //
 // Every mbarrier wait is bounded (global timer); on expiry the CTA drains its async
 // copies and MMAs, frees its tensor memory, writes VITFE_EDEVICE_TIMEOUT and exits.
@@ -69,9 +69,11 @@ struct EmbedArgs {
   int bn, nstage, npass;
   int tmem_cols;
   int num_tiles;   // 256-row pair tiles
-  // work units: each pair tile's npass N passes in `split` groups of ppu passes (split > 1
-  // only when there are fewer tiles than CTA pairs); unit u = tile * split + group
-  int split, ppu, num_units;
+  // work units: tiles [0, whole_tiles) are one unit each (all npass N passes); every later
+  // tile is `split` units of ppu passes each (unit whole_tiles + (tile - whole_tiles) *
+  // split + group), so that a last round holding fewer tiles than CTA pairs is spread
+  // over the pairs
+  int whole_tiles, split, ppu, num_units;
   uint64_t limit_ns;
   int stall_w_loads;       // test hook: the weight producer issues nothing
   // 2D-RoPE rows written by the same launch (null: embeddings only)
@@ -110,6 +112,21 @@ __device__ __forceinline__ int tile_kind(int r0, const SmemHdr* h, int T) {
   for (int i = i0; i <= i1; ++i)
     if (!tab_bit(h->still, i) && !tab_bit(h->bad, i)) return kStream;
   return kResident;
+}
+
+// Tile and N-pass range [p_lo, p_hi) of work unit u.
+__device__ __forceinline__ void unit_range(const EmbedArgs& a, int u, int& tile, int& p_lo, int& p_hi) {
+  if (u < a.whole_tiles) {
+    tile = u;
+    p_lo = 0;
+    p_hi = a.npass;
+    return;
+  }
+  const int v = u - a.whole_tiles;
+  const int g = v % a.split;
+  tile = a.whole_tiles + v / a.split;
+  p_lo = g * a.ppu;
+  p_hi = min(a.npass, p_lo + a.ppu);
 }
 
 // Number of K16 MMA steps of block j of a slice (the last block may be partial).
@@ -477,15 +494,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t np = 0;
     bool ok = true;
     int u = cid;
-    RowSrc cur = u < args.num_units ? row_src<P>(args, hs, (u / args.split) * kPairRows + rofs)
+    auto tile_of = [&](int uu) {
+      int t, lo, hi;
+      unit_range(args, uu, t, lo, hi);
+      return t;
+    };
+    RowSrc cur = u < args.num_units ? row_src<P>(args, hs, tile_of(u) * kPairRows + rofs)
                                     : RowSrc{nullptr, 0, 0};
     if (half == 0) prefetch_row<P>(cur, args.T);
     for (; ok && u < args.num_units; u += ncl) {
-      const int tile = u / args.split;
-      const int npu = min(args.ppu, args.npass - (u - tile * args.split) * args.ppu);   // passes of the unit
+      int tile, p_lo, p_hi;
+      unit_range(args, u, tile, p_lo, p_hi);
+      const int npu = p_hi - p_lo;   // passes of the unit
       const int kind = tile_kind(tile * kPairRows, hs, args.T);
       const int next = u + ncl;
-      const RowSrc nxt = next < args.num_units ? row_src<P>(args, hs, (next / args.split) * kPairRows + rofs)
+      const RowSrc nxt = next < args.num_units ? row_src<P>(args, hs, tile_of(next) * kPairRows + rofs)
                                                : RowSrc{nullptr, 0, 0};
       if (kind != kPad) {
         const int nprod = (kind == kResident) ? 1 : npu * args.T;
@@ -513,9 +536,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t nb = 0, stage = 0, bphase = 0;
       bool ok = true;
       for (int u = cid; ok && u < args.num_units; u += ncl) {
-        const int tile = u / args.split;
-        const int p_lo = (u - tile * args.split) * args.ppu;
-        const int p_hi = min(args.npass, p_lo + args.ppu);
+        int tile, p_lo, p_hi;
+        unit_range(args, u, tile, p_lo, p_hi);
         const int kind = tile_kind(tile * kPairRows, hs, args.T);
         if (kind == kPad) continue;
         // folded still tiles: one slice of the folded weight per block
@@ -609,9 +631,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } while (0)
 
       for (int u = cid; ok && u < args.num_units; u += ncl) {
-        const int tile = u / args.split;
-        const int p_lo = (u - tile * args.split) * args.ppu;
-        const int p_hi = min(args.npass, p_lo + args.ppu);
+        int tile, p_lo, p_hi;
+        unit_range(args, u, tile, p_lo, p_hi);
         const int kind = tile_kind(tile * kPairRows, hs, args.T);
         if (kind == kPad) continue;
         for (int p = p_lo; ok && p < p_hi; ++p) {
@@ -685,9 +706,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t na = 0;
     bool ok = true;
     for (int u = cid; ok && u < args.num_units; u += ncl) {
-      const int tile = u / args.split;
-      const int p_lo = (u - tile * args.split) * args.ppu;
-      const int p_hi = min(args.npass, p_lo + args.ppu);
+      int tile, p_lo, p_hi;
+      unit_range(args, u, tile, p_lo, p_hi);
       const int r0 = tile * kPairRows;
       const int kind = tile_kind(r0, hs, args.T);
       const int r = r0 + rloc;
@@ -855,16 +875,20 @@ cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_byte
   a.tmem_cols = 32;
   while (a.tmem_cols < 2 * c.bn) a.tmem_cols <<= 1;
   a.num_tiles = (int)((rows + kPairRows - 1) / kPairRows);
-  // fewer tiles than CTA pairs: spread each tile's N passes over several pairs (each
-  // produces the tile's A itself), so a small batch is not one pair's five passes in a row
+  // The tiles of a last round that would leave CTA pairs idle (all tiles of a batch with
+  // fewer tiles than pairs) have their N passes spread over several pairs, each of which
+  // produces the tile's A itself: a round of few tiles is then not one pair's five passes
+  // in a row.  The passes of a tile give the same results on whichever pair runs them.
   {
-    int split = 1;
-    if (a.num_tiles > 0 && a.num_tiles < c.max_clusters) split = c.max_clusters / a.num_tiles;
+    const int R = c.max_clusters;
+    const int rem = a.num_tiles % R;
+    int split = rem > 0 ? R / rem : 1;
     if (split > a.npass) split = a.npass;
     if (split < 1) split = 1;
     a.ppu = (a.npass + split - 1) / split;
     a.split = (a.npass + a.ppu - 1) / a.ppu;
-    a.num_units = a.num_tiles * a.split;
+    a.whole_tiles = a.num_tiles - rem;
+    a.num_units = a.whole_tiles + rem * a.split;
   }
   a.limit_ns = c.wait_limit_ns;
   a.stall_w_loads = c.test_stall_w_loads ? 1 : 0;
