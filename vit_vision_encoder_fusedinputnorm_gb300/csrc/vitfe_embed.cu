@@ -137,6 +137,32 @@ __host__ __device__ constexpr int ksteps_of(int j) {
   return rem >= 64 ? 4 : (rem + 15) / 16;
 }
 
+// Where the K blocks of A live.  Patch 16 keeps the last two blocks of each producer half
+// in tensor memory, beside accumulators of at most 192 columns each: the 64 KB that frees
+// in shared memory holds six more W stages.  Patch 14 keeps every block in shared memory.
+constexpr uint32_t kTmemACol = 384;   // first tensor-memory column of the A blocks
+template <int P>
+__host__ __device__ constexpr int ntm_blocks() { return P == 16 ? 4 : 0; }
+template <int P>
+__host__ __device__ constexpr int nblk_of() { return (3 * P * P + 63) / 64; }
+template <int P>
+__host__ __device__ constexpr bool in_tmem(int j) {
+  constexpr int H = nblk_of<P>() / 2, Q = ntm_blocks<P>() / 2;
+  return Q > 0 && (j % H) >= H - Q;
+}
+// tensor-memory column of block j (in_tmem), 32 columns per block
+template <int P>
+__host__ __device__ constexpr uint32_t tm_col(int j) {
+  constexpr int H = nblk_of<P>() / 2, Q = ntm_blocks<P>() / 2;
+  return kTmemACol + 32u * (uint32_t)((j / H) * Q + (j % H) - (H - Q));
+}
+// shared-memory slot of block j (!in_tmem)
+template <int P>
+__host__ __device__ constexpr int smem_slot(int j) {
+  constexpr int H = nblk_of<P>() / 2, Q = ntm_blocks<P>() / 2;
+  return (j / H) * (H - Q) + (j % H);
+}
+
 // Order in which the MMA consumes (and, in a tile's last pass, releases) the K blocks of
 // a slice: 0, NBLK/2, 1, NBLK/2 + 1, ...  The two producer threads of a row fill blocks
 // [0, NBLK/2) and [NBLK/2, NBLK) in parallel, so this order consumes both halves at the
@@ -181,7 +207,7 @@ template <int P, int JB, int JE>
 __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, uint32_t a_smem,
                                                SmemHdr* hs, uint32_t np, int row, const float sc[3],
                                                const float sh[3], volatile int* abort_flag,
-                                               uint64_t limit_ns, uint32_t a_full_leader) {
+                                               uint64_t limit_ns, uint32_t a_full_leader, uint32_t tmem_a) {
   constexpr int RUN = 3 * P;                 // bytes of one patch row of pixels
   constexpr int KS = 3 * P * P;
   constexpr int NBLK = (KS + 63) / 64;
@@ -245,6 +271,7 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
     if (lo_ + 1 < hi_ && lo_ + 1 < P && !(DEFER && lo_ + 1 == R0 + 2)) VITFE_LOAD_ROW(lo_ + 1);
   }
   if (!mbar_wait_cl(a_empty0 + 8u * JB, empty_parity, abort_flag, limit_ns, 128)) return false;
+  if (in_tmem<P>(JB)) tc_fence_after();
 
 #pragma unroll
   for (int ph = R0; ph <= P; ++ph) {
@@ -283,20 +310,33 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
         const int kc = kw >> 2;                // chunk of 8 features
         const int j = kc >> 3;                 // K block
         const int q = kc & 7;                  // chunk inside the 128-byte row
-        const uint32_t addr = a_smem + (uint32_t)j * kABlockBytes + row_off + (((uint32_t)q ^ swz) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(cw[0]), "r"(cw[1]), "r"(cw[2]),
-                     "r"(cw[3])
-                     : "memory");
+        if (in_tmem<P>(j)) {
+          // four columns of this thread's tensor-memory lane (warp-collective)
+          tmem_st_32x32b_x4(tmem_a + tm_col<P>(j) + 4u * (uint32_t)q, cw[0], cw[1], cw[2], cw[3]);
+        } else {
+          const uint32_t addr =
+              a_smem + (uint32_t)smem_slot<P>(j) * kABlockBytes + row_off + (((uint32_t)q ^ swz) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(cw[0]), "r"(cw[1]), "r"(cw[2]),
+                       "r"(cw[3])
+                       : "memory");
+        }
         if (q == 7 || kc == KEND / 8 - 1) {
-          // this thread's generic-proxy writes to its own CTA's shared memory become
-          // visible to the tensor core; one release arrive per warp on the even CTA
-          fence_proxy_async_smem();
+          // this thread's writes become visible to the tensor core (generic-proxy shared
+          // memory: proxy fence; tensor memory: wait for the stores, then the tcgen05
+          // fence); one release arrive per warp on the even CTA
+          if (in_tmem<P>(j)) {
+            tmem_wait_st();
+            tc_fence_before();
+          } else {
+            fence_proxy_async_smem();
+          }
           __syncwarp();
           if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(a_full_leader + 8u * (uint32_t)j);
           if (j + 1 < JE) {
             VITFE_ROWS_OF_BLOCK(j + 1);
             if (!mbar_wait_cl(a_empty0 + 8u * (uint32_t)(j + 1), empty_parity, abort_flag, limit_ns, 128))
               return false;
+            if (in_tmem<P>(j + 1)) tc_fence_after();
           }
         }
       }
@@ -423,14 +463,13 @@ template <int P>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     embed_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_wf,
                  const EmbedArgs args) {
-  constexpr int KS = 3 * P * P;
-  constexpr int NBLK = (KS + 63) / 64;
+  constexpr int NBLK = nblk_of<P>();
   extern __shared__ uint8_t smem_raw[];
   SmemHdr* hs = reinterpret_cast<SmemHdr*>(smem_raw);
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t tiles_base = (raw_base + (uint32_t)sizeof(SmemHdr) + 1023u) & ~1023u;
   const uint32_t a_smem = tiles_base;
-  const uint32_t b_smem = tiles_base + NBLK * kABlockBytes;
+  const uint32_t b_smem = tiles_base + (NBLK - ntm_blocks<P>()) * kABlockBytes;
   const int bnh = args.bn / 2;                                   // W rows per CTA per tile
   const uint32_t b_stage_bytes = (uint32_t)bnh * 128u;
 
@@ -491,6 +530,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int row = threadIdx.x & (kProducerThreads - 1);
     const int half = threadIdx.x / kProducerThreads;
     const int rofs = (int)rank * kTileM + row;
+    // this warp's lane quarter of the tensor-memory A blocks
+    const uint32_t tmem_a = hs->tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
     uint32_t np = 0;
     bool ok = true;
     int u = cid;
@@ -517,10 +558,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint8_t* base = cur.base0 ? cur.base0 + cur.fstride * s : nullptr;
           if (half == 0)
             ok = produce_blocks<P, 0, NBLK / 2>(base, cur.rs, a_smem, hs, np, row, sc, sh, abort_flag,
-                                                args.limit_ns, a_full_L);
+                                                args.limit_ns, a_full_L, tmem_a);
           else
             ok = produce_blocks<P, NBLK / 2, NBLK>(base, cur.rs, a_smem, hs, np, row, sc, sh, abort_flag,
-                                                   args.limit_ns, a_full_L);
+                                                   args.limit_ns, a_full_L, tmem_a);
           ++np;
           if (q == 0 && half == 0) prefetch_row<P>(nxt, args.T);
         }
@@ -609,15 +650,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #define VITFE_WAIT_A(J)                                                                       \
   do {                                                                                        \
     if (!mbar_wait_warp<true>(a_full0 + 8u * (J), np & 1u, abort_flag, args.limit_ns)) ok = false; \
+    if (in_tmem<P>(J)) tc_fence_after();                                                      \
   } while (0)
-#define VITFE_STEP(ADESC, NK, FIRST)                                                          \
+// one stage: the K16 MMAs of block J (A in shared memory at descriptor ADESC, or in
+// tensor memory) against the stage's W image, then the stage's release
+#define VITFE_STEP(J, ADESC, NK, FIRST)                                                       \
   do {                                                                                        \
     const uint64_t bd_ = bd_cur;                                                              \
     if (elect_one()) {                                                                        \
-      umma_bf16_pair(d_tmem, (ADESC), bd_, idesc, (FIRST) ? 0u : 1u);                         \
-      if ((NK) > 1) umma_bf16_pair(d_tmem, (ADESC) + 2u, bd_ + 2u, idesc, 1u);               \
-      if ((NK) > 2) umma_bf16_pair(d_tmem, (ADESC) + 4u, bd_ + 4u, idesc, 1u);               \
-      if ((NK) > 3) umma_bf16_pair(d_tmem, (ADESC) + 6u, bd_ + 6u, idesc, 1u);               \
+      if (in_tmem<P>(J)) {                                                                    \
+        const uint32_t ta_ = tmem + tm_col<P>(J);                                             \
+        umma_bf16_pair_ta(d_tmem, ta_, bd_, idesc, (FIRST) ? 0u : 1u);                        \
+        if ((NK) > 1) umma_bf16_pair_ta(d_tmem, ta_ + 8u, bd_ + 2u, idesc, 1u);              \
+        if ((NK) > 2) umma_bf16_pair_ta(d_tmem, ta_ + 16u, bd_ + 4u, idesc, 1u);             \
+        if ((NK) > 3) umma_bf16_pair_ta(d_tmem, ta_ + 24u, bd_ + 6u, idesc, 1u);             \
+      } else {                                                                                \
+        umma_bf16_pair(d_tmem, (ADESC), bd_, idesc, (FIRST) ? 0u : 1u);                       \
+        if ((NK) > 1) umma_bf16_pair(d_tmem, (ADESC) + 2u, bd_ + 2u, idesc, 1u);             \
+        if ((NK) > 2) umma_bf16_pair(d_tmem, (ADESC) + 4u, bd_ + 4u, idesc, 1u);             \
+        if ((NK) > 3) umma_bf16_pair(d_tmem, (ADESC) + 6u, bd_ + 6u, idesc, 1u);             \
+      }                                                                                       \
       umma_commit_pair(b_empty0 + 8u * stage);                                                \
     }                                                                                         \
     __syncwarp();                                                                             \
@@ -652,11 +704,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int jj = 0; jj < NBLK; ++jj) {
               const int j = blk_order<NBLK>(jj);
               if (p == p_lo) VITFE_WAIT_A(j);   // the unit's first pass meets the fresh A
-              const uint64_t ad = adesc0 + (uint64_t)(j * (kABlockBytes >> 4));
+              const uint64_t ad = adesc0 + (uint64_t)(smem_slot<P>(j) * (kABlockBytes >> 4));
               for (int sl = 0; ok && sl < Ts; ++sl) {
                 VITFE_WAIT_B();
                 if (!ok) break;
-                VITFE_STEP(ad, ksteps_of<P>(j), j == 0 && sl == 0);
+                VITFE_STEP(j, ad, ksteps_of<P>(j), j == 0 && sl == 0);
               }
               if (!ok) break;
               if (p == p_hi - 1) {
@@ -672,7 +724,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 VITFE_WAIT_A(j);
                 VITFE_WAIT_B();
                 if (!ok) break;
-                VITFE_STEP(adesc0 + (uint64_t)(j * (kABlockBytes >> 4)), ksteps_of<P>(j), sl == 0 && j == 0);
+                VITFE_STEP(j, adesc0 + (uint64_t)(smem_slot<P>(j) * (kABlockBytes >> 4)), ksteps_of<P>(j),
+                           sl == 0 && j == 0);
                 if (elect_one()) umma_commit_pair(a_empty0 + 8u * j);
                 __syncwarp();
               }
@@ -788,6 +841,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ---- teardown ------------------------------------------------------------
   __syncwarp();
+  // a producer that left on a timeout may still have tensor-memory stores in flight
+  if (ntm_blocks<P>() > 0 && warp < kProducerWarps) tmem_wait_st();
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
@@ -812,13 +867,15 @@ cudaError_t embed_configure(Ctx& c) {
   int max_optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
   if (e != cudaSuccess) return e;
-  // widest N tile first (fewest MMA issues per flop); a stage holds this CTA's half of
-  // one W tile, and at least two stages must fit beside the resident A slice
-  for (int bn : {256, 128}) {
+  // widest N tile first (fewest MMA issues per flop; patch 16: at most 192, so that two
+  // accumulators leave tensor-memory room for its A blocks); a stage holds this CTA's half
+  // of one W tile, and at least two stages must fit beside the shared-memory A blocks
+  const int ntm = c.P == 16 ? ntm_blocks<16>() : ntm_blocks<14>();
+  for (int bn : {c.P == 16 ? 192 : 256, 128}) {
     if (bn > c.N && bn != 128) continue;
     const int b = bn < c.N ? bn : c.N;
     for (int nst = 8; nst >= 2 && !c.embed_ok; --nst) {
-      const size_t need = embed_smem_bytes(c.nblk, b / 2, nst);
+      const size_t need = embed_smem_bytes(c.nblk - ntm, b / 2, nst);
       if (need <= (size_t)max_optin) {
         c.bn = b;
         c.nstage = nst;
@@ -874,6 +931,7 @@ cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_byte
   a.npass = (c.N + c.bn - 1) / c.bn;
   a.tmem_cols = 32;
   while (a.tmem_cols < 2 * c.bn) a.tmem_cols <<= 1;
+  if (c.P == 16) a.tmem_cols = 512;   // A blocks from column kTmemACol
   a.num_tiles = (int)((rows + kPairRows - 1) / kPairRows);
   // The tiles of a last round that would leave CTA pairs idle (all tiles of a batch with
   // fewer tiles than pairs) have their N passes spread over several pairs, each of which
