@@ -12,12 +12,14 @@
 //   warps 0-7   A producers: two threads per tile row (each half of the K blocks) gather
 //               uint8 pixel runs with aligned 4-byte loads, normalise in fp32, round to
 //               bf16 and store into 128-byte-swizzled K-major shared-memory blocks (64
-//               features each);
+//               features each); with patch 16 the last two blocks of each half go to
+//               tensor memory instead (tcgen05.st), and the MMA reads them from there;
 //   warp 12     TMA producer of this CTA's half of each W tile: one box copies one
 //               shared-memory image of the pre-tiled weight (bn/8 rows of 512 bytes);
 //   warp 13     tensor-memory allocation (both CTAs); in the even CTA the whole warp runs
 //               the MMA issue loop and one elected lane issues (fp32 accumulators
-//               double-buffered in tensor memory);
+//               double-buffered in tensor memory; N passes of 256 columns, or 192 with
+//               patch 16 so that the A blocks fit beside them);
 //   warps 8-11  epilogue, one warp per tensor-memory lane quarter: tcgen05.ld of the
 //               accumulator, + bias, bf16 RNE, 256-bit stores; in a vitfe_embed_rope
 //               launch also the tile's 2D-RoPE rows.
