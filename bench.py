@@ -211,8 +211,13 @@ def kernel_only(args):
     from vit_vision_encoder_fusedinputnorm_gb300.frontend import FrontEnd
     from vit_vision_encoder_fusedinputnorm_gb300 import binding as B
     vbuild.build()
-    wl = synth.make_workload(CFG, item_subset=list(range(args.images)))
-    wl.items = wl.items[:args.images]
+    if args.cfg == 4:
+        # the patch-16 workload: its first 65,536-row bucket of stills
+        wl = synth.make_workload(4)
+        wl.items = [wl.items[i] for i in wl.buckets[0]]
+    else:
+        wl = synth.make_workload(args.cfg, item_subset=list(range(args.images)))
+        wl.items = wl.items[:args.images]
     fe = FrontEnd.from_workload(wl)
     b = fe.upload(wl.items)
     st = fe.status_tensor()
@@ -252,6 +257,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cfg", type=int, default=CFG,
+                    help="--kernel-only workload: 2 (first --images stills of the throughput set) or 4 (patch-16 bucket)")
     ap.add_argument("--kernel-only", choices=["embed", "embed_rope", "rope", "rope_apply", "normalize_patchify"],
                     help="profiling mode: launch one entry point on a subset of the images, print nothing")
     ap.add_argument("--images", type=int, default=64, help="images of the workload (profiling mode)")
