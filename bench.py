@@ -476,7 +476,10 @@ def main():
                      "frac_of_sustained": achieved / float(pk.get("bf16_tflops_sustained", peak)),
                      "kernel": "embed_kernel<14>", "flops_per_launch": flops,
                      "kernel_ms": embed_ms},
-        "side_paths": {"unfused_embed_then_rope_ms": unfused_ms,
+        "side_paths": {"timing": ("median of isolated launches, each waited for before the next (the GPU idles "
+                                  "between them, so its clock recovers); the step above is a back-to-back loop "
+                                  "at the power cap, so the two are not directly comparable"),
+                       "unfused_embed_then_rope_ms": unfused_ms,
                        "patch16_bucket_embed": {"rows": p16_rows, "ms": p16_ms, "tflops": p16_tflops,
                                                 "frac_of_peak": p16_tflops / float(pk["bf16_tflops"]),
                                                 "graph_replay_embed_rope_ms": p16_graph_ms,
