@@ -628,11 +628,13 @@ def test_embed_rope_host_reports_errors():
     fe.close()
 
 
-def test_bounded_wait_runs_out_and_reports_timeout(monkeypatch):
+@pytest.mark.parametrize("patch", [14, 16])
+def test_bounded_wait_runs_out_and_reports_timeout(monkeypatch, patch):
     # failure detection without a fault: a handle whose weight producer issues no loads
     # (test hook) leaves the MMA's wait unsatisfied; after the short limit every role leaves,
-    # the launch reports VITFE_EDEVICE_TIMEOUT, and the context keeps working
-    wl = synth.small_workload(61, [(1, 4, 6, 1), (2, 2, 4, 4)], patch=14, hidden=256, head_dim=80)
+    # the launch reports VITFE_EDEVICE_TIMEOUT, and the context keeps working (patch 16:
+    # its producers also write A blocks into tensor memory)
+    wl = synth.small_workload(61, [(1, 4, 6, 1), (2, 2, 4, 4)], patch=patch, hidden=256, head_dim=80)
     monkeypatch.setenv("VITFE_WAIT_LIMIT_MS", "200")
     monkeypatch.setenv("VITFE_TEST_STALL_W_LOADS", "1")
     stalled = _fe(wl)
