@@ -544,9 +544,9 @@ __host__ __device__ constexpr int np_stage_rs(int P, int KW) {
 template <int P, int T>
 struct NpPair {
   static constexpr int RUN = 3 * P;                 // bytes of one pixel row of one patch
-  static constexpr int NW = (RUN + 3) / 4 + 1;      // aligned words covering it
-  uint32_t raw[T][NW];
-  uint32_t sft;                                     // byte offset of the run in raw[.][0]
+  static constexpr int NC = (RUN + 7 + 7) / 8;      // aligned 8-byte chunks covering it
+  uint32_t raw[T][2 * NC];
+  uint32_t sft[T];                                  // byte offset of the run in raw[t][0] (0..7)
   int flag;                                         // bit 0: row valid, bit 1: still item
   int nrows;                                        // rows of this pair inside [0, rows)
 };
@@ -586,15 +586,21 @@ __device__ __forceinline__ void np_fetch(NpPair<P, T>& q, const NpArgs& a, const
   const long long mfs = __shfl_sync(0xffffffffu, fs, lr);
   if (lr >= q.nrows) q.flag = 0;
   const uintptr_t addr0 = (uintptr_t)(base + (unsigned long long)(mrs * ph));
-  q.sft = (uint32_t)(addr0 & 3u);
 #pragma unroll
   for (int tt = 0; tt < T; ++tt) {
-    // a still's one frame serves every temporal slice: load it once
+    // a still's one frame serves every temporal slice: load it once.  8-byte loads (each
+    // chunk holds a byte of the run, so none leaves the buffer): half the load instructions
+    // of 4-byte ones on the load/store pipe that bounds this kernel
     const bool ld = (q.flag & 1) && (tt == 0 || !(q.flag & 2));
-    const uint32_t* w0 = reinterpret_cast<const uint32_t*>((addr0 + (uintptr_t)(mfs * tt)) & ~uintptr_t(3));
+    const uintptr_t at = addr0 + (uintptr_t)(mfs * tt);
+    q.sft[tt] = (uint32_t)(at & 7u);
+    const uint2* c0 = reinterpret_cast<const uint2*>(at & ~uintptr_t(7));
 #pragma unroll
-    for (int w = 0; w < NpPair<P, T>::NW; ++w)
-      q.raw[tt][w] = (ld && 4u * w < q.sft + NpPair<P, T>::RUN) ? __ldg(w0 + w) : 0u;
+    for (int c = 0; c < NpPair<P, T>::NC; ++c) {
+      const uint2 v = (ld && 8u * c < q.sft[tt] + NpPair<P, T>::RUN) ? __ldg(c0 + c) : make_uint2(0u, 0u);
+      q.raw[tt][2 * c] = v.x;
+      q.raw[tt][2 * c + 1] = v.y;
+    }
   }
 }
 
@@ -605,13 +611,19 @@ __device__ __forceinline__ void np_convert(const NpPair<P, T>& q, uint32_t* srow
   constexpr int NA = (3 * P + 3) / 4;
   const bool valid = q.flag & 1;
   const bool still = q.flag & 2;
-  const uint32_t sel = 0x3210u + 0x1111u * q.sft;
+  static_assert(NA + 1 < 2 * NpPair<P, T>::NC, "the 4-byte view of a run lies inside its chunks");
 #pragma unroll
   for (int tt = 0; tt < T; ++tt) {
     if (tt > 0 && still) break;
+    const uint32_t sel = 0x3210u + 0x1111u * (q.sft[tt] & 3u);
+    const bool hi = q.sft[tt] >= 4u;   // the run's aligned words start one word into the chunks
     uint32_t al[NA];
 #pragma unroll
-    for (int w = 0; w < NA; ++w) al[w] = __byte_perm(q.raw[tt][w], q.raw[tt][w + 1], sel);
+    for (int w = 0; w < NA; ++w) {
+      const uint32_t x0 = hi ? q.raw[tt][w + 1] : q.raw[tt][w];
+      const uint32_t x1 = hi ? q.raw[tt][w + 2] : q.raw[tt][w + 1];
+      al[w] = __byte_perm(x0, x1, sel);
+    }
 #pragma unroll
     for (int c = 0; c < 3; ++c) {
       const uint64_t s2 = pack2(__float_as_uint(sc[c]), __float_as_uint(sc[c]));
@@ -652,7 +664,7 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int P, int T>
-__global__ void __launch_bounds__(kAuxThreads) normalize_patchify_p_kernel(const NpArgs a) {
+__global__ void __launch_bounds__(kAuxThreads, 3) normalize_patchify_p_kernel(const NpArgs a) {
   constexpr int KW = 3 * T * P * P / 2;                     // bf16 pairs per row
   constexpr int RS = np_stage_rs(P, KW);
   static_assert(KW % 4 == 0 && RS % 4 == 0, "16-byte rows");
