@@ -544,9 +544,13 @@ __host__ __device__ constexpr int np_stage_rs(int P, int KW) {
 template <int P, int T>
 struct NpPair {
   static constexpr int RUN = 3 * P;                 // bytes of one pixel row of one patch
-  static constexpr int NC = (RUN + 7 + 7) / 8;      // aligned 8-byte chunks covering it
-  uint32_t raw[T][2 * NC];
-  uint32_t sft[T];                                  // byte offset of the run in raw[t][0] (0..7)
+  // aligned chunks of CB bytes covering it: 16 when runs start on 16-byte bounds in the
+  // usual layout (3P a multiple of 16), else 8 (fewer selects to realign scattered runs)
+  static constexpr int CB = (RUN % 16 == 0) ? 16 : 8;
+  static constexpr int NC = (RUN + CB - 1 + CB - 1) / CB;
+  static constexpr int NWR = NC * CB / 4;           // words held
+  uint32_t raw[T][NWR];
+  uint32_t sft[T];                                  // byte offset of the run in raw[t][0] (< CB)
   int flag;                                         // bit 0: row valid, bit 1: still item
   int nrows;                                        // rows of this pair inside [0, rows)
 };
@@ -592,14 +596,25 @@ __device__ __forceinline__ void np_fetch(NpPair<P, T>& q, const NpArgs& a, const
     // chunk holds a byte of the run, so none leaves the buffer): half the load instructions
     // of 4-byte ones on the load/store pipe that bounds this kernel
     const bool ld = (q.flag & 1) && (tt == 0 || !(q.flag & 2));
+    constexpr int CB = NpPair<P, T>::CB;
     const uintptr_t at = addr0 + (uintptr_t)(mfs * tt);
-    q.sft[tt] = (uint32_t)(at & 7u);
-    const uint2* c0 = reinterpret_cast<const uint2*>(at & ~uintptr_t(7));
+    q.sft[tt] = (uint32_t)(at & (CB - 1));
 #pragma unroll
     for (int c = 0; c < NpPair<P, T>::NC; ++c) {
-      const uint2 v = (ld && 8u * c < q.sft[tt] + NpPair<P, T>::RUN) ? __ldg(c0 + c) : make_uint2(0u, 0u);
-      q.raw[tt][2 * c] = v.x;
-      q.raw[tt][2 * c + 1] = v.y;
+      const bool hit = ld && (uint32_t)(CB * c) < q.sft[tt] + NpPair<P, T>::RUN;
+      if constexpr (CB == 16) {
+        const uint4* c0 = reinterpret_cast<const uint4*>(at & ~uintptr_t(15));
+        const uint4 v = hit ? __ldg(c0 + c) : make_uint4(0u, 0u, 0u, 0u);
+        q.raw[tt][4 * c] = v.x;
+        q.raw[tt][4 * c + 1] = v.y;
+        q.raw[tt][4 * c + 2] = v.z;
+        q.raw[tt][4 * c + 3] = v.w;
+      } else {
+        const uint2* c0 = reinterpret_cast<const uint2*>(at & ~uintptr_t(7));
+        const uint2 v = hit ? __ldg(c0 + c) : make_uint2(0u, 0u);
+        q.raw[tt][2 * c] = v.x;
+        q.raw[tt][2 * c + 1] = v.y;
+      }
     }
   }
 }
@@ -611,19 +626,28 @@ __device__ __forceinline__ void np_convert(const NpPair<P, T>& q, uint32_t* srow
   constexpr int NA = (3 * P + 3) / 4;
   const bool valid = q.flag & 1;
   const bool still = q.flag & 2;
-  static_assert(NA + 1 < 2 * NpPair<P, T>::NC, "the 4-byte view of a run lies inside its chunks");
+  constexpr int WMAX = NpPair<P, T>::CB / 4 - 1;   // largest word offset of a run in its chunks
+  static_assert(NA + WMAX < NpPair<P, T>::NWR, "the 4-byte view of a run lies inside its chunks");
 #pragma unroll
   for (int tt = 0; tt < T; ++tt) {
     if (tt > 0 && still) break;
     const uint32_t sel = 0x3210u + 0x1111u * (q.sft[tt] & 3u);
-    const bool hi = q.sft[tt] >= 4u;   // the run's aligned words start one word into the chunks
+    // the run's aligned words start wo words into the chunks: v[k] = raw[wo + k]
+    const uint32_t wo = q.sft[tt] >> 2;
+    uint32_t v[NA + 1];
+#pragma unroll
+    for (int k = 0; k <= NA; ++k) {
+      const uint32_t a01 = (wo & 1u) ? q.raw[tt][k + 1] : q.raw[tt][k];
+      if constexpr (WMAX >= 2) {
+        const uint32_t a23 = (wo & 1u) ? q.raw[tt][k + 3] : q.raw[tt][k + 2];
+        v[k] = (wo & 2u) ? a23 : a01;
+      } else {
+        v[k] = a01;
+      }
+    }
     uint32_t al[NA];
 #pragma unroll
-    for (int w = 0; w < NA; ++w) {
-      const uint32_t x0 = hi ? q.raw[tt][w + 1] : q.raw[tt][w];
-      const uint32_t x1 = hi ? q.raw[tt][w + 2] : q.raw[tt][w + 1];
-      al[w] = __byte_perm(x0, x1, sel);
-    }
+    for (int w = 0; w < NA; ++w) al[w] = __byte_perm(v[w], v[w + 1], sel);
 #pragma unroll
     for (int c = 0; c < 3; ++c) {
       const uint64_t s2 = pack2(__float_as_uint(sc[c]), __float_as_uint(sc[c]));
