@@ -382,6 +382,21 @@ def main():
                     ts.append(a0.elapsed_time(a1))
         return statistics.median(ts)
 
+    def looped(fn, n=50, warm=5):
+        """Mean time per launch over a back-to-back loop (steady-state bandwidth of the
+        short HBM-bound kernels, whose launch gaps the isolated timing would count)."""
+        with torch.cuda.stream(stream):
+            for _ in range(warm):
+                fn()
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(n):
+                fn()
+            a1.record(stream)
+            a1.synchronize()
+        return a0.elapsed_time(a1) / n
+
     # the two calls the fused launch replaces, and the RoPE expansion alone (HBM-write bound)
     def unfused():
         B.vitfe_embed(fe.h, batch.pixels, batch.pixel_bytes, batch.items, batch.n_items, batch.capacity, rows,
@@ -394,13 +409,21 @@ def main():
     # to bf16), timed for reference only; it is never the headline
     folded_ms = timed(lambda: B.vitfe_embed_folded(fe.h, batch.pixels, batch.pixel_bytes, batch.items,
                                                    batch.n_items, batch.capacity, rows, out, None, stream))
-    rope_ms = timed(lambda: B.vitfe_rope(fe.h, batch.items, batch.n_items, batch.capacity, rows, wl.head_dim,
-                                         wl.theta, cos, sin, None, stream))
+    def rope_call():
+        B.vitfe_rope(fe.h, batch.items, batch.n_items, batch.capacity, rows, wl.head_dim, wl.theta, cos, sin,
+                     None, stream)
+
+    rope_iso_ms = timed(rope_call)
+    rope_ms = looped(rope_call)
 
     # standalone normalise + patchify (HBM-bound side path), timed alone
     flat = torch.empty((rows, K), dtype=torch.bfloat16, device=dev)
-    np_ms = timed(lambda: B.vitfe_normalize_patchify(fe.h, batch.pixels, batch.pixel_bytes, batch.items,
-                                                     batch.n_items, batch.capacity, rows, flat, None, stream))
+    def np_call():
+        B.vitfe_normalize_patchify(fe.h, batch.pixels, batch.pixel_bytes, batch.items, batch.n_items,
+                                   batch.capacity, rows, flat, None, stream)
+
+    np_iso_ms = timed(np_call)
+    np_ms = looped(np_call)
     np_bytes = batch.pixel_bytes + rows * K * 2
 
     # the patch-16 bucket workload (Qwen3-VL-like: K 1536, N 1152): one 65,536-row bucket of
@@ -451,8 +474,11 @@ def main():
     # buffer), from the step's cos/sin tables: HBM bound, in place
     heads = N // wl.head_dim
     qkv = torch.zeros((rows, 3 * N), dtype=torch.bfloat16, device=dev)
-    apply_ms = timed(lambda: B.vitfe_rope_apply(cos, sin, rows, wl.head_dim, qkv, heads, 3 * N, qkv[:, N:],
-                                                heads, 3 * N, stream))
+    def apply_call():
+        B.vitfe_rope_apply(cos, sin, rows, wl.head_dim, qkv, heads, 3 * N, qkv[:, N:], heads, 3 * N, stream)
+
+    apply_iso_ms = timed(apply_call)
+    apply_ms = looped(apply_call)
     apply_bytes = rows * (2 * heads * wl.head_dim * 2 * 2 + wl.head_dim // 2 * 4 * 2)
     del qkv
     del flat
@@ -476,9 +502,11 @@ def main():
                      "frac_of_sustained": achieved / float(pk.get("bf16_tflops_sustained", peak)),
                      "kernel": "embed_kernel<14>", "flops_per_launch": flops,
                      "kernel_ms": embed_ms},
-        "side_paths": {"timing": ("median of isolated launches, each waited for before the next (the GPU idles "
-                                  "between them, so its clock recovers); the step above is a back-to-back loop "
-                                  "at the power cap, so the two are not directly comparable"),
+        "side_paths": {"timing": ("rope, rope_apply_qk and normalize_patchify (HBM bound): mean over a "
+                                  "back-to-back loop of 50 launches, like the step; their *_isolated_ms and the "
+                                  "other side paths: median of isolated launches, each waited for before the "
+                                  "next (the GPU idles between them, so launch latency counts and the clock "
+                                  "recovers)"),
                        "unfused_embed_then_rope_ms": unfused_ms,
                        "patch16_bucket_embed": {"rows": p16_rows, "ms": p16_ms, "tflops": p16_tflops,
                                                 "frac_of_peak": p16_tflops / float(pk["bf16_tflops"]),
@@ -490,12 +518,15 @@ def main():
                                                 "note": "approximation (W slices summed, rounded once to bf16); "
                                                         "K 588 for stills; not the method's exact result"},
                        "rope_ms": rope_ms,
+                       "rope_isolated_ms": rope_iso_ms,
                        "rope_gbs": rows * wl.head_dim // 2 * 4 * 2 / (rope_ms / 1e3) / 1e9,
                        "rope_frac_hbm": rows * wl.head_dim // 2 * 4 * 2 / (rope_ms / 1e3) / 1e9 / float(pk["hbm_gbs"]),
                        "rope_apply_qk_ms": apply_ms,
+                       "rope_apply_qk_isolated_ms": apply_iso_ms,
                        "rope_apply_qk_gbs": apply_bytes / (apply_ms / 1e3) / 1e9,
                        "rope_apply_qk_frac_hbm": apply_bytes / (apply_ms / 1e3) / 1e9 / float(pk["hbm_gbs"]),
                        "normalize_patchify_ms": np_ms,
+                       "normalize_patchify_isolated_ms": np_iso_ms,
                        "normalize_patchify_gbs": np_bytes / (np_ms / 1e3) / 1e9,
                        "normalize_patchify_frac_hbm": np_bytes / (np_ms / 1e3) / 1e9 / float(pk["hbm_gbs"])},
         "e2e": {"value": world * rows / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
