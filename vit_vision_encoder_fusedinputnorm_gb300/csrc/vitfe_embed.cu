@@ -31,7 +31,8 @@
 // at create.  The whole slice of A (all K blocks) stays resident in shared memory
 // while the tile loops over the N passes; for stills the temporal slices are equal,
 // so one resident slice feeds the MMAs of every slice ("resident" tiles).  Tiles
-// holding video rows re-produce A per (pass, slice) ("stream" tiles).
+// holding video rows re-produce A per slice ("stream" tiles), once for each pair of N
+// passes: every A block then feeds both tensor-memory accumulators before it is freed.
 //
 // The K blocks are consumed in the order the producer threads fill them (one block of each
 // producer range in turn).  The work unit is (pair tile, group of N passes): the tiles of
@@ -554,7 +555,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const RowSrc nxt = next < args.num_units ? row_src<P>(args, hs, tile_of(next) * kPairRows + rofs)
                                                : RowSrc{nullptr, 0, 0};
       if (kind != kPad) {
-        const int nprod = (kind == kResident) ? 1 : npu * args.T;
+        // stream tiles: one production of each slice per pair of N passes
+        const int nprod = (kind == kResident) ? 1 : ((npu + 1) / 2) * args.T;
         for (int q = 0; ok && q < nprod; ++q) {
           const int s = (kind == kResident) ? 0 : (q % args.T);
           const uint8_t* base = cur.base0 ? cur.base0 + cur.fstride * s : nullptr;
@@ -588,12 +590,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int Ts = fold ? 1 : args.T;
         const CUtensorMap* map = fold ? &tmap_wf : &tmap_w;
         const int nsteps = Ts * NBLK;
-        for (int p = p_lo; ok && p < p_hi; ++p) {
-          // this CTA's images of pass p: (p, rank, slice, block), bnh/4 rows of 512 B each
-          const int blk0 = (p * 2 + (int)rank) * Ts * NBLK;
-          for (int st = 0; ok && st < nsteps; ++st) {
-            const int j = blk_order<NBLK>((kind == kResident) ? st / Ts : st % NBLK);
-            const int sl = (kind == kResident) ? st % Ts : st / NBLK;
+        for (int p = p_lo; ok && p < p_hi;) {
+          // the MMA's pairs of stream passes take, per (slice, block), both passes' images
+          const int G = (kind == kStream && p + 1 < p_hi) ? 2 : 1;
+          for (int st = 0; ok && st < nsteps * G; ++st) {
+            int j, sl, pg;
+            if (kind == kResident) {
+              j = blk_order<NBLK>(st / Ts);
+              sl = st % Ts;
+              pg = p;
+            } else {
+              const int s2 = st / G;
+              j = blk_order<NBLK>(s2 % NBLK);
+              sl = s2 / NBLK;
+              pg = p + st % G;
+            }
+            // this CTA's image (pass pg, rank, slice, block), bnh/4 rows of 512 B each
+            const int blk0 = (pg * 2 + (int)rank) * Ts * NBLK;
             if (!mbar_wait_cl(smem_u32(&hs->b_empty[stage]), bphase ^ 1u, abort_flag, args.limit_ns)) {
               ok = false;
               break;
@@ -604,6 +617,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ++nb;
             if (++stage == (uint32_t)args.nstage) { stage = 0; bphase ^= 1u; }
           }
+          p += G;
         }
       }
       if (!ok) {
@@ -656,21 +670,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } while (0)
 // one stage: the K16 MMAs of block J (A in shared memory at descriptor ADESC, or in
 // tensor memory) against the stage's W image, then the stage's release
-#define VITFE_STEP(J, ADESC, NK, FIRST)                                                       \
+#define VITFE_STEP(D, ID, J, ADESC, NK, FIRST)                                                \
   do {                                                                                        \
     const uint64_t bd_ = bd_cur;                                                              \
     if (elect_one()) {                                                                        \
       if (in_tmem<P>(J)) {                                                                    \
         const uint32_t ta_ = tmem + tm_col<P>(J);                                             \
-        umma_bf16_pair_ta(d_tmem, ta_, bd_, idesc, (FIRST) ? 0u : 1u);                        \
-        if ((NK) > 1) umma_bf16_pair_ta(d_tmem, ta_ + 8u, bd_ + 2u, idesc, 1u);              \
-        if ((NK) > 2) umma_bf16_pair_ta(d_tmem, ta_ + 16u, bd_ + 4u, idesc, 1u);             \
-        if ((NK) > 3) umma_bf16_pair_ta(d_tmem, ta_ + 24u, bd_ + 6u, idesc, 1u);             \
+        umma_bf16_pair_ta((D), ta_, bd_, (ID), (FIRST) ? 0u : 1u);                            \
+        if ((NK) > 1) umma_bf16_pair_ta((D), ta_ + 8u, bd_ + 2u, (ID), 1u);                  \
+        if ((NK) > 2) umma_bf16_pair_ta((D), ta_ + 16u, bd_ + 4u, (ID), 1u);                 \
+        if ((NK) > 3) umma_bf16_pair_ta((D), ta_ + 24u, bd_ + 6u, (ID), 1u);                 \
       } else {                                                                                \
-        umma_bf16_pair(d_tmem, (ADESC), bd_, idesc, (FIRST) ? 0u : 1u);                       \
-        if ((NK) > 1) umma_bf16_pair(d_tmem, (ADESC) + 2u, bd_ + 2u, idesc, 1u);             \
-        if ((NK) > 2) umma_bf16_pair(d_tmem, (ADESC) + 4u, bd_ + 4u, idesc, 1u);             \
-        if ((NK) > 3) umma_bf16_pair(d_tmem, (ADESC) + 6u, bd_ + 6u, idesc, 1u);             \
+        umma_bf16_pair((D), (ADESC), bd_, (ID), (FIRST) ? 0u : 1u);                           \
+        if ((NK) > 1) umma_bf16_pair((D), (ADESC) + 2u, bd_ + 2u, (ID), 1u);                 \
+        if ((NK) > 2) umma_bf16_pair((D), (ADESC) + 4u, bd_ + 4u, (ID), 1u);                 \
+        if ((NK) > 3) umma_bf16_pair((D), (ADESC) + 6u, bd_ + 6u, (ID), 1u);                 \
       }                                                                                       \
       umma_commit_pair(b_empty0 + 8u * stage);                                                \
     }                                                                                         \
@@ -689,15 +703,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         unit_range(args, u, tile, p_lo, p_hi);
         const int kind = tile_kind(tile * kPairRows, hs, args.T);
         if (kind == kPad) continue;
-        for (int p = p_lo; ok && p < p_hi; ++p) {
-          const uint32_t buf = na & 1u;
-          if (!mbar_wait_warp<true>(smem_u32(&hs->acc_empty[buf]), ((na >> 1) & 1u) ^ 1u, abort_flag, args.limit_ns)) {
-            ok = false;
-            break;
+        for (int p = p_lo; ok && p < p_hi;) {
+          // a stream tile's N passes go in pairs, one accumulator each, so that every
+          // production of its A (both temporal slices) feeds two passes
+          const int G = (kind == kStream && p + 1 < p_hi) ? 2 : 1;
+          for (int g = 0; ok && g < G; ++g) {
+            const uint32_t n_ = na + (uint32_t)g;
+            if (!mbar_wait_warp<true>(smem_u32(&hs->acc_empty[n_ & 1u]), ((n_ >> 1) & 1u) ^ 1u, abort_flag,
+                                      args.limit_ns))
+              ok = false;
           }
+          if (!ok) break;
           tc_fence_after();
-          const int npw = min(args.bn, args.N - p * args.bn);
-          const uint32_t idesc = idesc_bf16(kPairRows, npw);
+          const uint32_t buf = na & 1u;
+          const uint32_t idesc = idesc_bf16(kPairRows, min(args.bn, args.N - p * args.bn));
           const uint32_t d_tmem = tmem + buf * (uint32_t)args.bn;
           if (kind == kResident) {
             // one resident slice of A feeds every temporal slice of W (one folded slice)
@@ -710,7 +729,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               for (int sl = 0; ok && sl < Ts; ++sl) {
                 VITFE_WAIT_B();
                 if (!ok) break;
-                VITFE_STEP(j, ad, ksteps_of<P>(j), j == 0 && sl == 0);
+                VITFE_STEP(d_tmem, idesc, j, ad, ksteps_of<P>(j), j == 0 && sl == 0);
               }
               if (!ok) break;
               if (p == p_hi - 1) {
@@ -719,15 +738,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               }
             }
           } else {
+            // the pair's second pass (G == 2): the other accumulator
+            const uint32_t idesc1 = idesc_bf16(kPairRows, min(args.bn, args.N - (p + 1) * args.bn));
+            const uint32_t d_tmem1 = tmem + (buf ^ 1u) * (uint32_t)args.bn;
             for (int sl = 0; ok && sl < T; ++sl) {
 #pragma unroll
               for (int jj = 0; jj < NBLK; ++jj) {
                 const int j = blk_order<NBLK>(jj);
+                const uint64_t ad = adesc0 + (uint64_t)(smem_slot<P>(j) * (kABlockBytes >> 4));
                 VITFE_WAIT_A(j);
-                VITFE_WAIT_B();
+                // one copy of the issue code for both passes (code size: the issue loop is
+                // sensitive to instruction fetch)
+#pragma unroll 1
+                for (int g = 0; g < G; ++g) {
+                  VITFE_WAIT_B();
+                  if (!ok) break;
+                  VITFE_STEP(g ? d_tmem1 : d_tmem, g ? idesc1 : idesc, j, ad, ksteps_of<P>(j), sl == 0 && j == 0);
+                }
                 if (!ok) break;
-                VITFE_STEP(j, adesc0 + (uint64_t)(smem_slot<P>(j) * (kABlockBytes >> 4)), ksteps_of<P>(j),
-                           sl == 0 && j == 0);
                 if (elect_one()) umma_commit_pair(a_empty0 + 8u * j);
                 __syncwarp();
               }
@@ -735,9 +763,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          if (elect_one()) umma_commit_pair(smem_u32(&hs->acc_full[buf]));
+          if (elect_one()) {
+            for (int g = 0; g < G; ++g) umma_commit_pair(smem_u32(&hs->acc_full[(na + (uint32_t)g) & 1u]));
+          }
           __syncwarp();
-          ++na;
+          na += (uint32_t)G;
+          p += G;
         }
         if (kind == kResident) ++np;
       }
