@@ -159,8 +159,8 @@ vitfe_status vitfe_embed_folded(vitfe_t h, const uint8_t* pixels, int64_t pixel_
                                 cudaStream_t stream);
 
 /* vitfe_embed and vitfe_rope over the same items in one launch: the embed
- * kernel's epilogue warps write each tile's cos/sin rows while the tile's first
- * accumulator is computed.  Arguments, outputs, pad rows and errors are those of
+ * kernel's epilogue warps write each tile's cos/sin rows after draining the tile's
+ * second N pass, while the MMAs of its later passes run.  Arguments, outputs, pad rows and errors are those of
  * the two calls, with one status word; items with h or w > VITFE_ROPE_MAX_SIDE
  * are rejected on the device for both outputs.  The first call with a
  * (head_dim, theta) pair also launches the table build (see vitfe_rope). */
