@@ -799,8 +799,11 @@ __global__ void tile_weight_kernel(const __nv_bfloat16* __restrict__ W, const __
   const int bnh = bn / 2;
   const int npass = (N + bn - 1) / bn;
   const int TL = fold ? 1 : T;                 // slices in the layout
+  const bool shared_tail = w_tail_shared(kslice);
+  const int nfb = shared_tail ? kslice / 64 : nblk;   // blocks with one image per slice
+  const int imgs = w_images(kslice, TL);              // images per (pass, CTA half)
   const long long per_blk = (long long)bnh * 64;
-  const long long total = (long long)npass * 2 * TL * nblk * per_blk;
+  const long long total = (long long)npass * 2 * imgs * per_blk;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
     const long long blk = idx / per_blk;
@@ -808,14 +811,24 @@ __global__ void tile_weight_kernel(const __nv_bfloat16* __restrict__ W, const __
     const int i = within >> 6;
     const int qp = (within >> 3) & 7;                 // physical chunk in the row
     const int e = ((qp ^ (i & 7)) << 3) | (within & 7);
-    const int j = (int)(blk % nblk);
-    const int sl = (int)((blk / nblk) % TL);
-    const int r = (int)((blk / ((long long)nblk * TL)) & 1);
-    const int p = (int)(blk / ((long long)nblk * TL * 2));
+    const int g = (int)(blk % imgs);
+    const int r = (int)((blk / imgs) & 1);
+    const int p = (int)(blk / ((long long)imgs * 2));
     const int npw = min(bn, N - p * bn);
-    const int kp = 64 * j + e;
+    int sl, kp;
+    bool inside;
+    if (shared_tail && g == TL * nfb) {
+      // the slices' tails: slice e / 16 at K16 offset e / 16
+      sl = e >> 4;
+      kp = 64 * nfb + (e & 15);
+      inside = sl < TL && kp < kslice;
+    } else {
+      sl = g / nfb;
+      kp = 64 * (g % nfb) + e;
+      inside = kp < kslice;
+    }
     __nv_bfloat16 v = __float2bfloat16_rn(0.0f);
-    if (i < npw / 2 && kp < kslice) {
+    if (i < npw / 2 && inside) {
       const int n = p * bn + r * (npw / 2) + i;
       const int ph = kp / (3 * P);
       const int rem = kp - ph * 3 * P;

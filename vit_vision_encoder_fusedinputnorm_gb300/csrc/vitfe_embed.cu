@@ -467,6 +467,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     embed_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_wf,
                  const EmbedArgs args) {
   constexpr int NBLK = nblk_of<P>();
+  constexpr bool kSharedTail = w_tail_shared(3 * P * P);         // the slices' tails share an image
+  constexpr int kNfb = kSharedTail ? (3 * P * P) / 64 : NBLK;    // blocks with one image per slice
   extern __shared__ uint8_t smem_raw[];
   SmemHdr* hs = reinterpret_cast<SmemHdr*>(smem_raw);
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -589,33 +591,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const bool fold = args.folded && kind == kResident;
         const int Ts = fold ? 1 : args.T;
         const CUtensorMap* map = fold ? &tmap_wf : &tmap_w;
-        const int nsteps = Ts * NBLK;
+        // this CTA's image of (pass pg, slice sl, block j): bnh/4 rows of 512 B each; the
+        // slices' one-step tails share one image (w_images)
+        const int imgs = w_images(3 * P * P, Ts);
+        auto img_of = [&](int pg, int sl, int j) {
+          const int base = (pg * 2 + (int)rank) * imgs;
+          return (kSharedTail && j == kNfb) ? base + Ts * kNfb : base + sl * kNfb + j;
+        };
+        auto load_image = [&](int img) {
+          if (!mbar_wait_cl(smem_u32(&hs->b_empty[stage]), bphase ^ 1u, abort_flag, args.limit_ns)) {
+            ok = false;
+            return;
+          }
+          if (leader) mbar_arrive_expect_tx(smem_u32(&hs->b_full[stage]), 2u * b_stage_bytes);
+          tma_load_2d_pair(b_smem + stage * b_stage_bytes, map, b_full_L + 8u * stage, 0, img * (bnh / 4));
+          ++nb;
+          if (++stage == (uint32_t)args.nstage) { stage = 0; bphase ^= 1u; }
+        };
         for (int p = p_lo; ok && p < p_hi;) {
           // the MMA's pairs of stream passes take, per (slice, block), both passes' images
           const int G = (kind == kStream && p + 1 < p_hi) ? 2 : 1;
-          for (int st = 0; ok && st < nsteps * G; ++st) {
-            int j, sl, pg;
-            if (kind == kResident) {
-              j = blk_order<NBLK>(st / Ts);
-              sl = st % Ts;
-              pg = p;
-            } else {
-              const int s2 = st / G;
-              j = blk_order<NBLK>(s2 % NBLK);
-              sl = s2 / NBLK;
-              pg = p + st % G;
+          if (kind == kResident) {
+            for (int jj = 0; ok && jj < NBLK; ++jj) {
+              const int j = blk_order<NBLK>(jj);
+              const int nsl = (kSharedTail && j == kNfb) ? 1 : Ts;   // one image holds every tail
+              for (int sl = 0; ok && sl < nsl; ++sl) load_image(img_of(p, sl, j));
             }
-            // this CTA's image (pass pg, rank, slice, block), bnh/4 rows of 512 B each
-            const int blk0 = (pg * 2 + (int)rank) * Ts * NBLK;
-            if (!mbar_wait_cl(smem_u32(&hs->b_empty[stage]), bphase ^ 1u, abort_flag, args.limit_ns)) {
-              ok = false;
-              break;
-            }
-            if (leader) mbar_arrive_expect_tx(smem_u32(&hs->b_full[stage]), 2u * b_stage_bytes);
-            tma_load_2d_pair(b_smem + stage * b_stage_bytes, map, b_full_L + 8u * stage, 0,
-                             (blk0 + sl * NBLK + j) * (bnh / 4));
-            ++nb;
-            if (++stage == (uint32_t)args.nstage) { stage = 0; bphase ^= 1u; }
+          } else {
+            for (int sl = 0; ok && sl < Ts; ++sl)
+              for (int jj = 0; ok && jj < NBLK; ++jj)
+                for (int g = 0; ok && g < G; ++g) load_image(img_of(p + g, sl, blk_order<NBLK>(jj)));
           }
           p += G;
         }
@@ -669,10 +674,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (in_tmem<P>(J)) tc_fence_after();                                                      \
   } while (0)
 // one stage: the K16 MMAs of block J (A in shared memory at descriptor ADESC, or in
-// tensor memory) against the stage's W image, then the stage's release
-#define VITFE_STEP(D, ID, J, ADESC, NK, FIRST)                                                \
+// tensor memory) against the stage's W image from K16 step BOFF / 2 on, then the stage's
+// release
+#define VITFE_STEP(D, ID, J, ADESC, NK, FIRST, BOFF)                                          \
   do {                                                                                        \
-    const uint64_t bd_ = bd_cur;                                                              \
+    const uint64_t bd_ = bd_cur + (uint64_t)(BOFF);                                           \
     if (elect_one()) {                                                                        \
       if (in_tmem<P>(J)) {                                                                    \
         const uint32_t ta_ = tmem + tm_col<P>(J);                                             \
@@ -686,6 +692,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if ((NK) > 2) umma_bf16_pair((D), (ADESC) + 4u, bd_ + 4u, (ID), 1u);                 \
         if ((NK) > 3) umma_bf16_pair((D), (ADESC) + 6u, bd_ + 6u, (ID), 1u);                 \
       }                                                                                       \
+      umma_commit_pair(b_empty0 + 8u * stage);                                                \
+    }                                                                                         \
+    __syncwarp();                                                                             \
+    if (++stage == nstage) {                                                                  \
+      stage = 0;                                                                              \
+      bphase ^= 1u;                                                                           \
+      bd_cur = bdesc0;                                                                        \
+    } else {                                                                                  \
+      bd_cur += bstep;                                                                        \
+    }                                                                                         \
+  } while (0)
+
+// one stage holding the NS temporal slices' one-step tails: each slice's K16 MMA against
+// the same A block, slice s at K16 step s of the image (never a pass's first MMA)
+#define VITFE_STEP_TAILS(D, ID, ADESC, NS)                                                    \
+  do {                                                                                        \
+    const uint64_t bd_ = bd_cur;                                                              \
+    if (elect_one()) {                                                                        \
+      for (int s_ = 0; s_ < (NS); ++s_) umma_bf16_pair((D), (ADESC), bd_ + 2u * (uint64_t)s_, (ID), 1u); \
       umma_commit_pair(b_empty0 + 8u * stage);                                                \
     }                                                                                         \
     __syncwarp();                                                                             \
@@ -726,10 +751,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const int j = blk_order<NBLK>(jj);
               if (p == p_lo) VITFE_WAIT_A(j);   // the unit's first pass meets the fresh A
               const uint64_t ad = adesc0 + (uint64_t)(smem_slot<P>(j) * (kABlockBytes >> 4));
-              for (int sl = 0; ok && sl < Ts; ++sl) {
+              if (kSharedTail && j == kNfb) {
                 VITFE_WAIT_B();
                 if (!ok) break;
-                VITFE_STEP(d_tmem, idesc, j, ad, ksteps_of<P>(j), j == 0 && sl == 0);
+                VITFE_STEP_TAILS(d_tmem, idesc, ad, Ts);
+              } else {
+                for (int sl = 0; ok && sl < Ts; ++sl) {
+                  VITFE_WAIT_B();
+                  if (!ok) break;
+                  VITFE_STEP(d_tmem, idesc, j, ad, ksteps_of<P>(j), j == 0 && sl == 0, 0u);
+                }
               }
               if (!ok) break;
               if (p == p_hi - 1) {
@@ -753,7 +784,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int g = 0; g < G; ++g) {
                   VITFE_WAIT_B();
                   if (!ok) break;
-                  VITFE_STEP(g ? d_tmem1 : d_tmem, g ? idesc1 : idesc, j, ad, ksteps_of<P>(j), sl == 0 && j == 0);
+                  VITFE_STEP(g ? d_tmem1 : d_tmem, g ? idesc1 : idesc, j, ad, ksteps_of<P>(j), sl == 0 && j == 0,
+                             (kSharedTail && j == kNfb) ? 2u * (uint32_t)sl : 0u);
                 }
                 if (!ok) break;
                 if (elect_one()) umma_commit_pair(a_empty0 + 8u * j);
@@ -772,6 +804,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (kind == kResident) ++np;
       }
+#undef VITFE_STEP_TAILS
 #undef VITFE_STEP
 #undef VITFE_WAIT_A
 #undef VITFE_WAIT_B

@@ -216,8 +216,9 @@ vitfe_status vitfe_create(vitfe_t* out, const float mean[3], const float std_[3]
   }
   if (c.embed_ok) {
     const size_t npass = (size_t)((c.N + c.bn - 1) / c.bn);
-    c.w_tile_bytes = npass * 2 * (size_t)c.T * (size_t)c.nblk * (size_t)(c.bn / 2) * 128;
-    c.w_tile_f_bytes = c.T > 1 ? c.w_tile_bytes / (size_t)c.T : 0;
+    const size_t img_bytes = (size_t)(c.bn / 2) * 128;
+    c.w_tile_bytes = npass * 2 * (size_t)vitfe::w_images(c.kslice, c.T) * img_bytes;
+    c.w_tile_f_bytes = c.T > 1 ? npass * 2 * (size_t)vitfe::w_images(c.kslice, 1) * img_bytes : 0;
     if (cudaMalloc(&c.w_tile, c.w_tile_bytes) != cudaSuccess ||
         (c.w_tile_f_bytes > 0 && cudaMalloc(&c.w_tile_f, c.w_tile_f_bytes) != cudaSuccess)) {
       cudaGetLastError();

@@ -353,6 +353,16 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "r"(taddr));
 }
 
+// Weight images per (N pass, CTA half) for TL temporal slices of kslice features: one per
+// (slice, 64-feature block), except that when the last block of a slice holds at most 16
+// features (one K16 step) the TL slices' tails share one image, slice s at K16 offset s.
+__host__ __device__ constexpr bool w_tail_shared(int kslice) {
+  return (kslice % 64) != 0 && (kslice % 64) <= 16;
+}
+__host__ __device__ constexpr int w_images(int kslice, int TL) {
+  return w_tail_shared(kslice) ? TL * (kslice / 64) + 1 : TL * ((kslice + 63) / 64);
+}
+
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes,
 // 8-row core groups 1024 bytes apart (tile base 1024-byte aligned).
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
