@@ -88,3 +88,33 @@ def test_gather_restores_the_input_order_on_two_gloo_ranks(patches, dtype):
     want = torch.cat([_rows_of(i, n, width, dtype) for i, n in enumerate(patches)]).float().numpy()
     for r in range(world):
         assert np.array_equal(results[r], want)
+
+
+def _single(rank, port, results):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=0, world_size=1)
+    try:
+        patches = [3, 5]
+        a = dp.assign_by_patches(patches, 1)
+        local = torch.cat([_rows_of(i, n, 4, torch.float32) for i, n in enumerate(patches)])
+        results["same"] = bool(torch.equal(dp.gather_in_input_order(local, patches, a), local))
+        try:
+            dp.gather_in_input_order(local[:-1], patches, a)
+            results["short"] = "no error"
+        except ValueError:
+            results["short"] = "ValueError"
+        try:
+            dp.gather_in_input_order(local, patches, [[0], [1]])
+            results["lists"] = "no error"
+        except ValueError:
+            results["lists"] = "ValueError"
+    finally:
+        dist.destroy_process_group()
+
+
+def test_gather_on_one_rank_is_the_identity_and_checks_its_arguments():
+    results = mp.Manager().dict()
+    mp.spawn(_single, args=(_free_port(), results), nprocs=1, join=True)
+    assert results["same"] is True
+    assert results["short"] == "ValueError"   # local rows must match the rank's items
+    assert results["lists"] == "ValueError"   # one item list per rank
