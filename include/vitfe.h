@@ -36,9 +36,10 @@
  *    the embed kernel load no weights, to exercise that path in tests.
  *  - Bucket padding: rows at or past sum(t*h*w) up to `rows` are written as
  *    embedding 0, cos 1, sin 0, position id -1, flatten_patches 0.
- *  - Pixel reads: the library reads whole aligned 4-byte words that overlap
- *    an item's bytes, so it may touch up to 3 bytes past `pixel_bytes` but
- *    never a word that holds none of the item's bytes.
+ *  - Pixel reads: the library reads whole aligned words of 4, 8 or 16 bytes
+ *    that each hold at least one of an item's bytes, so it may touch up to 15
+ *    bytes past `pixel_bytes` (inside the same 16-byte-aligned block of the
+ *    16-byte-aligned buffer) but never a word that holds none of them.
  */
 #ifndef VITFE_H
 #define VITFE_H
