@@ -665,6 +665,9 @@ SHAPES = {
     "p14_t2_m1": (14, 2, 1, [(1, 3, 5, 1), (2, 1, 3, 4), (1, 7, 1, 1)]),     # no merge grouping
     "p14_t2_m4": (14, 2, 4, [(1, 4, 8, 1), (2, 4, 4, 4)]),                   # 4 x 4 merge units
     "p8_t2_m2": (8, 2, 2, [(1, 4, 6, 1), (2, 2, 4, 4)]),                     # no embed kernel for patch 8
+    # three and four temporal slices: the slices' one-step tails share one weight image
+    "p14_t3_m2": (14, 3, 2, [(1, 2, 4, 1), (1, 4, 2, 3)]),
+    "p14_t4_m2": (14, 4, 2, [(1, 4, 6, 1), (2, 2, 4, 8)]),
 }
 
 
