@@ -45,6 +45,24 @@ def peaks():
     return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0), "fallback"
 
 
+def datasheet_fracs(path, achieved_tflops, hbm_gbs_by_path):
+    """Fractions of a datasheet's peaks, when a JSON file supplies them (nothing is
+    hard-coded): {"bf16_tflops": T, "hbm_gbs": B}, either key optional.  Returns None
+    without a file."""
+    if not path:
+        return None
+    with open(path) as f:
+        ds = json.load(f)
+    out = {"file": os.path.basename(path)}
+    if ds.get("bf16_tflops"):
+        out["bf16_tflops"] = float(ds["bf16_tflops"])
+        out["frac"] = achieved_tflops / float(ds["bf16_tflops"])
+    if ds.get("hbm_gbs"):
+        out["hbm_gbs"] = float(ds["hbm_gbs"])
+        out["hbm_fracs"] = {k: v / float(ds["hbm_gbs"]) for k, v in hbm_gbs_by_path.items()}
+    return out
+
+
 def source_hash() -> str:
     """Hash of the embed kernel's code (comments and whitespace stripped, so that editing a
     comment does not disown the committed ncu traffic figure)."""
@@ -257,6 +275,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--datasheet", default=None,
+                    help="JSON file with datasheet peaks ({\"bf16_tflops\": ..., \"hbm_gbs\": ...}); "
+                         "adds fractions of them to the line")
     ap.add_argument("--cfg", type=int, default=CFG,
                     help="--kernel-only workload: 2 (first --images stills of the throughput set) or 4 (patch-16 bucket)")
     ap.add_argument("--kernel-only", choices=["embed", "embed_rope", "rope", "rope_apply", "normalize_patchify"],
@@ -502,6 +523,10 @@ def main():
                      "frac_of_sustained": achieved / float(pk.get("bf16_tflops_sustained", peak)),
                      "kernel": "embed_kernel<14>", "flops_per_launch": flops,
                      "kernel_ms": embed_ms},
+        "datasheet": datasheet_fracs(args.datasheet, achieved, {
+            "rope": rows * wl.head_dim // 2 * 4 * 2 / (rope_ms / 1e3) / 1e9,
+            "rope_apply_qk": apply_bytes / (apply_ms / 1e3) / 1e9,
+            "normalize_patchify": np_bytes / (np_ms / 1e3) / 1e9}),
         "side_paths": {"timing": ("rope, rope_apply_qk and normalize_patchify (HBM bound): mean over a "
                                   "back-to-back loop of 50 launches, like the step; their *_isolated_ms and the "
                                   "other side paths: median of isolated launches, each waited for before the "
