@@ -38,6 +38,14 @@ What it computes, step by step, with the passage each step follows:
    own): a still's equal temporal slices of A multiply the summed weight
    slices rounded once to bf16.
 
+Precision.  Everything is float64, with one option: FusedInputNorm emits the
+model dtype (step 1's source, 实现拆解 item 2), bf16 here, so the GEMM of the
+method receives the normalised pixels rounded to bf16.  ``bf16_input=True``
+(embedding functions) applies exactly that rounding (to nearest, ties to even)
+to A before the exact float64 GEMM; the default leaves A unrounded.  The first
+is the method's own result before its output cast, the second the plain
+mathematical value; the parity tests compare against both.
+
 Readings where the pages are silent (each also listed in the design notes):
 the first step's order is rescale, subtract the mean, divide by std; the
 rotary width is head_dim / 2; a padded bucket's rows past the live rows are
@@ -58,7 +66,7 @@ __all__ = [
     "rope_workload", "pos_ids_workload", "normalize_patchify_workload", "cu_seqlens",
     "cu_seqlens_workload", "rope_apply", "round_to_bf16_bits", "fold_still_weight", "embed_folded_item",
     "embed_folded_workload",
-    "patch_coords",
+    "patch_coords", "to_model_dtype",
 ]
 
 
@@ -140,6 +148,15 @@ def normalize_patchify_item(item_pixels: np.ndarray, t: int, h: int, w: int, *, 
     return patchify(normalize(item_pixels, mean, std, rescale), t, h, w, patch, tpatch, merge)
 
 
+def to_model_dtype(x: np.ndarray) -> np.ndarray:
+    """The normalised pixels as FusedInputNorm hands them on: rounded to the nearest bf16
+    (ties to even), returned as float64.
+
+    "PR #55370 完整报告", 实现拆解 item 2: the norm emits the model dtype.
+    """
+    return bf16_bits_to_f64(round_to_bf16_bits(x))
+
+
 # ---------------------------------------------------------------------------
 # 3. patch embedding (img2col GEMM)
 # ---------------------------------------------------------------------------
@@ -158,12 +175,18 @@ def embed_rows(A: np.ndarray, W_bits: np.ndarray, b_bits: Optional[np.ndarray]) 
 
 
 def embed_item(item_pixels, t, h, w, W_bits, b_bits, *, patch, tpatch, merge, mean, std,
-               rescale, rows: Optional[np.ndarray] = None) -> np.ndarray:
-    """Embeddings of one item (optionally only the given local rows)."""
+               rescale, rows: Optional[np.ndarray] = None, bf16_input: bool = False) -> np.ndarray:
+    """Embeddings of one item (optionally only the given local rows).
+
+    bf16_input: the GEMM receives the normalised pixels in the model dtype
+    (``to_model_dtype``) instead of unrounded.
+    """
     A = normalize_patchify_item(item_pixels, t, h, w, patch=patch, tpatch=tpatch, merge=merge,
                                 mean=mean, std=std, rescale=rescale)
     if rows is not None:
         A = A[np.asarray(rows)]
+    if bf16_input:
+        A = to_model_dtype(A)
     return embed_rows(A, W_bits, b_bits)
 
 
@@ -173,12 +196,12 @@ def _item_starts(items) -> np.ndarray:
 
 
 def embed_workload(wl, items: Optional[Sequence[int]] = None, bucket_rows: Optional[int] = None,
-                   sample: Optional[np.ndarray] = None) -> np.ndarray:
+                   sample: Optional[np.ndarray] = None, bf16_input: bool = False) -> np.ndarray:
     """Embeddings of the items ``items`` (default: all) packed in order.
 
     With ``bucket_rows`` the result has that many rows and the pad rows are 0.
     With ``sample`` (global row indices into the packed output) only those rows
-    are returned, in the given order.
+    are returned, in the given order.  ``bf16_input`` as in ``embed_item``.
     """
     idx = list(range(len(wl.items))) if items is None else list(items)
     its = [wl.items[i] for i in idx]
@@ -186,7 +209,7 @@ def embed_workload(wl, items: Optional[Sequence[int]] = None, bucket_rows: Optio
     live = int(starts[-1])
     total = live if bucket_rows is None else int(bucket_rows)
     common = dict(patch=wl.patch, tpatch=wl.tpatch, merge=wl.merge, mean=wl.mean,
-                  std=wl.std, rescale=wl.rescale)
+                  std=wl.std, rescale=wl.rescale, bf16_input=bf16_input)
     if sample is None:
         out = np.zeros((total, wl.hidden), dtype=np.float64)
         for j, it in enumerate(its):
@@ -213,7 +236,8 @@ def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 
     bf16 keeps 8 significant bits: with x = m * 2^e (0.5 <= |m| < 1, frexp), the
     result is rint(m * 2^8) * 2^(e - 8), rint rounding half to even; both steps
-    are exact in float64.  Normal-range inputs only (the folded weights).
+    are exact in float64.  Normal-range inputs only (the folded weights and the
+    normalised pixels; zero stays zero).
     """
     x = np.asarray(x, dtype=np.float64)
     m, e = np.frexp(x)
@@ -239,11 +263,14 @@ def fold_still_weight(W_bits: np.ndarray, tpatch: int, patch: int) -> np.ndarray
 
 
 def embed_folded_item(item_pixels, t, h, w, W_bits, b_bits, Wf_bits, *, patch, tpatch, merge, mean,
-                      std, rescale, still: bool) -> np.ndarray:
+                      std, rescale, still: bool, bf16_input: bool = False) -> np.ndarray:
     """Embeddings of one item in the folded-still variant: a still uses temporal
-    slice 0 of A against W' (fold_still_weight); a video uses step 3 unchanged."""
+    slice 0 of A against W' (fold_still_weight); a video uses step 3 unchanged.
+    ``bf16_input`` as in ``embed_item``."""
     A = normalize_patchify_item(item_pixels, t, h, w, patch=patch, tpatch=tpatch, merge=merge,
                                 mean=mean, std=std, rescale=rescale)
+    if bf16_input:
+        A = to_model_dtype(A)
     if not still:
         return embed_rows(A, W_bits, b_bits)
     A4 = A.reshape(A.shape[0], 3, tpatch, patch * patch)
@@ -251,7 +278,7 @@ def embed_folded_item(item_pixels, t, h, w, W_bits, b_bits, Wf_bits, *, patch, t
     return embed_rows(A0, Wf_bits, b_bits)
 
 
-def embed_folded_workload(wl, bucket_rows: Optional[int] = None) -> np.ndarray:
+def embed_folded_workload(wl, bucket_rows: Optional[int] = None, bf16_input: bool = False) -> np.ndarray:
     Wf = fold_still_weight(wl.W_bits, wl.tpatch, wl.patch)
     starts = _item_starts(wl.items)
     total = int(starts[-1]) if bucket_rows is None else int(bucket_rows)
@@ -259,7 +286,8 @@ def embed_folded_workload(wl, bucket_rows: Optional[int] = None) -> np.ndarray:
     for j, it in enumerate(wl.items):
         out[starts[j]:starts[j + 1]] = embed_folded_item(
             it.pixels, it.t, it.h, it.w, wl.W_bits, wl.b_bits, Wf, patch=wl.patch, tpatch=wl.tpatch,
-            merge=wl.merge, mean=wl.mean, std=wl.std, rescale=wl.rescale, still=(it.frames == 1))
+            merge=wl.merge, mean=wl.mean, std=wl.std, rescale=wl.rescale, still=(it.frames == 1),
+            bf16_input=bf16_input)
     return out
 
 

@@ -12,6 +12,10 @@ rotary width) fails at least one of them:
 * patch embed: a direct Conv3d (kernel == stride) sum on tiny items, a one-hot
   weight that must return the normalised pixels exactly, and the constant
   colour closed form;
+* the model-dtype input of the GEMM (bf16_input): a one-hot weight returns the
+  pixels rounded to bf16, ties go to even, exact bf16 pixels pass unchanged,
+  the change is bounded by the cast's half spacings, and the constant colour
+  closed form with each channel rounded by brute force;
 * position ids: a hand-derived golden sequence and the closed-form index;
 * RoPE: pos 0, frequency index 0, the theta^(-1/2) frequency, geometric
   frequency ratio, angle addition between neighbouring positions,
@@ -280,6 +284,95 @@ def test_embed_workload_sample_and_bucket():
     assert np.all(full[wl.live_rows:] == 0)
     s = np.array([0, 5, 9, 8, 23, 17])
     assert np.array_equal(oracle.embed_workload(wl, sample=s), full[s])
+
+
+# ---------------------------------------------------------------- the model-dtype input of the GEMM
+
+def test_bf16_input_one_hot_returns_the_rounded_pixels():
+    # a one-hot weight passes A through: with bf16_input the outputs are the normalised
+    # pixels rounded to bf16 (to nearest, ties to even), and without it the exact values
+    P, T, m = 4, 2, 2
+    K = 3 * T * P * P
+    ks = [0, 5, 47, K - 1]
+    W = np.zeros((len(ks), K), np.uint16)
+    W[np.arange(len(ks)), ks] = 0x3F80
+    x = synth.position_coded_image(1, 2 * P, 4 * P)
+    kw = dict(patch=P, tpatch=T, merge=m, mean=synth.QWEN_MEAN, std=synth.QWEN_STD, rescale=synth.RESCALE)
+    exact = oracle.embed_item(x, 1, 2, 4, W, None, **kw)
+    cast = oracle.embed_item(x, 1, 2, 4, W, None, bf16_input=True, **kw)
+    A = oracle.normalize_patchify_item(x, 1, 2, 4, **kw)[:, ks]
+    assert np.array_equal(exact, A)
+    assert np.array_equal(cast, oracle.bf16_bits_to_f64(oracle.round_to_bf16_bits(A)))
+    assert np.any(cast != exact)
+
+
+def test_bf16_input_ties_go_to_even():
+    # mean -1, std 1, rescale 1/512: x = 1 + v/512, and the bf16 spacing in [1, 2) is 4/512.
+    # v = 2: halfway between 1 (even) and 1 + 4/512 -> 1; v = 6: halfway between 1 + 4/512
+    # (odd) and 1 + 8/512 (even) -> 1 + 8/512; v = 1, 3: nearest; v = 4: a bf16 value
+    P = 8
+    vals = [2, 6, 1, 3, 4]
+    x = np.zeros((1, P, P, 3), np.uint8)
+    x[0, 0, :len(vals), 0] = vals
+    W5 = np.zeros((len(vals), 3, P, P), np.uint16)
+    for n in range(len(vals)):
+        W5[n, 0, 0, n] = 0x3F80                                       # Conv3d order (c, ph, pw)
+    y = oracle.embed_item(x, 1, 1, 1, W5.reshape(len(vals), -1), None, patch=P, tpatch=1, merge=1,
+                          mean=(-1, -1, -1), std=(1, 1, 1), rescale=1 / 512, bf16_input=True)
+    assert y[0].tolist() == [1.0, 1 + 8 / 512, 1.0, 1 + 4 / 512, 1 + 4 / 512]
+    y = oracle.embed_item(x, 1, 1, 1, W5.reshape(len(vals), -1), None, patch=P, tpatch=1, merge=1,
+                          mean=(-1, -1, -1), std=(1, 1, 1), rescale=1 / 512)
+    assert y[0].tolist() == [1 + v / 512 for v in vals]
+
+
+def test_bf16_input_changes_nothing_when_the_pixels_are_bf16_values():
+    # rescale 1/256, mean 0, std 1: v / 256 has at most 8 significant bits, so the cast
+    # is exact and both oracles agree bit for bit
+    wl = synth.small_workload(12, [(1, 2, 4, 1), (2, 2, 2, 4)], patch=4, hidden=16)
+    wl.mean, wl.std, wl.rescale = (0.0, 0.0, 0.0), (1.0, 1.0, 1.0), 1 / 256
+    assert np.array_equal(oracle.embed_workload(wl, bf16_input=True), oracle.embed_workload(wl))
+
+
+def test_bf16_input_difference_is_bounded_by_the_cast():
+    # |y_cast - y| <= sum_k |W[n][k]| * (half a bf16 spacing at |x_k|) for every row and
+    # column, and the cast moves the results (a dropped or doubled rounding would not fit)
+    wl = synth.small_workload(13, [(1, 4, 6, 1), (2, 2, 2, 4)], patch=4, hidden=24)
+    y = oracle.embed_workload(wl)
+    yc = oracle.embed_workload(wl, bf16_input=True)
+    A = np.concatenate([oracle.normalize_patchify_item(it.pixels, it.t, it.h, it.w, patch=4, tpatch=2, merge=2,
+                                                       mean=wl.mean, std=wl.std, rescale=wl.rescale)
+                        for it in wl.items])
+    _, ex = np.frexp(np.abs(A))
+    half = np.ldexp(1.0, ex - 9)
+    bound = half @ np.abs(oracle.bf16_bits_to_f64(wl.W_bits)).T
+    d = np.abs(yc - y)
+    assert np.all(d <= bound * (1 + 1e-12))
+    assert d.max() > 0.05 * bound.max()
+
+
+def test_bf16_input_constant_colour_closed_form():
+    P, T, m, N = 4, 2, 2, 6
+    rng = np.random.default_rng(4)
+    W = synth.f32_to_bf16_bits(rng.standard_normal((N, 3 * T * P * P)).astype(np.float32) * 0.02)
+    b = synth.f32_to_bf16_bits(rng.standard_normal(N).astype(np.float32) * 0.02)
+    col = (31, 222, 140)
+    x = np.empty((1, 2 * P, 2 * P, 3), np.uint8)
+    x[...] = col
+    y = oracle.embed_item(x, 1, 2, 2, W, b, patch=P, tpatch=T, merge=m, mean=synth.QWEN_MEAN,
+                          std=synth.QWEN_STD, rescale=synth.RESCALE, bf16_input=True)
+    Wf = oracle.bf16_bits_to_f64(W).reshape(N, 3, -1).sum(axis=2)
+    xc = np.array([(col[c] / 255.0 - synth.QWEN_MEAN[c]) / synth.QWEN_STD[c] for c in range(3)])
+    # bf16 of each channel's value, from its own brute force over the bf16 grid near it
+    xb = []
+    for v in xc:
+        e = math.floor(math.log2(abs(v)))
+        step = 2.0 ** (e - 7)
+        lo = math.floor(v / step) * step
+        cands = [lo, lo + step]
+        best = min(cands, key=lambda c: (abs(c - v), (round(c / step) % 2)))
+        xb.append(best)
+    exp = Wf @ np.array(xb) + oracle.bf16_bits_to_f64(b)
+    assert np.allclose(y, exp[None, :], rtol=1e-12, atol=1e-13)
 
 
 # ---------------------------------------------------------------- position ids
