@@ -215,8 +215,10 @@ vitfe_status vitfe_cu_seqlens(vitfe_t h, const vitfe_item* items, const int32_t*
                               cudaStream_t stream);
 
 /* Allocation-free 2D-RoPE tables, for callers that cannot allocate device memory:
- * code under a memory pool it does not own, inside a CUDA-graph capture that must
- * not allocate, or in a process that may not call cudaMalloc after start-up.  No
+ * code whose device memory is all reserved up front by a pool it does not own (a
+ * serving runtime that carves up the GPU at start-up), or a process that may not call
+ * cudaMalloc once it is serving, where an allocation can fail or stall the other work
+ * on the GPU.  Creating a handle allocates, so they cannot use vitfe_rope.  No
  * counterpart in the pages; it computes exactly what vitfe_rope computes, without a
  * handle (tpatch and merge are passed directly).
  * Scratch: a 1 MiB file-scope device array that every GPU loading the library

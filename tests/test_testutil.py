@@ -27,13 +27,44 @@ def test_ulp_distance_across_zero():
     assert U.ulp_distance(a, b).tolist() == [2, 1, 1]
 
 
-def test_embed_errors_per_item():
+def test_rne_bf16_values_agrees_with_the_candidate_rounding():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(50000) * 10.0 ** rng.integers(-4, 2, 50000)
+    ties = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(2 + 2 ** -7), 0.0])
+    x = np.concatenate([x, ties])
+    assert np.array_equal(U.rne_bf16_values(x), U.bits_to_f64(U.f64_to_bf16_bits(x)))
+
+
+def test_beyond_rounding():
+    ulp = 2.0 ** -7                                # bf16 spacing in [1, 2); 2^-8 in [0.5, 1)
+    g = np.array([1.0, 1.0, 1.0, 1.0 + ulp, -1.0, 0.0, 1.0])
+    y = np.array([1.0 + ulp / 2, 1.0 + ulp, 1.0 - 2 ** -9, 1.0 + 0.5 * ulp, -(1.0 + 0.75 * ulp), 3e-3,
+                  1.0 - 2 ** -8])
+    got = U.beyond_rounding(g, y).tolist()
+    # rounds to g (tie, inside): 0; above by ulp: ulp - ulp/2; below 1.0 the spacing is
+    # 2^-8, so 1 - 2^-9 still rounds to 1 (tie to even) and 1 - 2^-8 lies 2^-9 beyond
+    assert got == [0.0, ulp / 2, 0.0, 0.0, 0.75 * ulp - ulp / 2, 3e-3, 2 ** -9]
+
+
+def test_embed_report_per_item_and_split():
     ref = np.ones((6, 4))
-    g = ref.copy()
-    g[4:] += 0.01
-    rel, mx = U.embed_errors(g, ref, [0, 4, 6])
-    # half a bf16 ulp at 1.0 is 2^-8
-    assert abs(rel - 0.01) < 1e-12 and abs(mx - (0.01 - 2 ** -8)) < 1e-12
+    ref_m = ref + 2 ** -10                         # the model-dtype cast moved the exact sum
+    g = np.ones((6, 4))
+    g[4:, 0] = 1.0 + 2 ** -7                       # one output a whole bf16 step up
+    rep = U.embed_report(g, ref, ref_m, [0, 4, 6])
+    assert rep["rows"] == 6 and rep["flips"] == 2
+    assert abs(rep["rel"] - np.sqrt(2 * 2 ** -14 / 8)) < 1e-12
+    assert rep["max_abs"] == 2 ** -7 - 2 ** -10 and rep["raw_max_abs"] == 2 ** -7
+    assert rep["cast"] == 2 ** -10 and rep["out_round"] == 2 ** -10 and rep["max_y"] == 1.0
+    assert rep["acc"] == 2 ** -7 - 2 ** -10 - 2 ** -8
+    U.check_embed(rep)
+    g[0, 0] = 1.0 + 2 ** -4 * 3                    # 0.1875 off
+    try:
+        U.check_embed(U.embed_report(g, ref, ref_m, [0, 4, 6]))
+    except AssertionError:
+        pass
+    else:
+        raise AssertionError("check_embed accepted an error of 0.19")
 
 
 def test_half_ulp():

@@ -991,8 +991,8 @@ cudaError_t launch_tile_weight(const Ctx& c, const __nv_bfloat16* W, const __nv_
 //
 // Some callers cannot allocate device memory at all: code running under an
 // allocator they do not own (a serving runtime whose memory pool is carved up in
-// advance, or a CUDA-graph capture that must not allocate), or a host process
-// that is forbidden to call cudaMalloc after start-up.  vitfe_rope needs a handle,
+// advance), or a host process that is forbidden to call cudaMalloc after start-up,
+// where an allocation can fail or stall the other work sharing the GPU.  vitfe_rope needs a handle,
 // and creating one allocates.  vitfe_rope_noalloc runs the same two RoPE kernels
 // with their axis-table scratch in the file-scope array below instead: 1 MiB,
 // enough for position tables up to VITFE_ROPE_MAX_SIDE positions and head_dim up
