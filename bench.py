@@ -1,11 +1,16 @@
 """Benchmark of the fused ViT front end (patch embeddings/s, % of dense bf16 peak).
 
 One step = one pass of the front end over 64 synthetic 1344x1344 stills
-(589,824 patches): the fused normalise + patchify + patch-embed GEMM + bias
-(vitfe_embed) and the 2D-RoPE tables (vitfe_rope), through the C ABI with
+(589,824 patches): the fused normalise + patchify + patch-embed GEMM + bias and
+the 2D-RoPE rows in one launch (vitfe_embed_rope), through the C ABI with
 inputs resident in device memory.  Inputs (347 MB of pixels) and outputs
 (1.51 GB of embeddings) exceed the 129 MB L2, so no flush is needed between
-iterations.
+iterations.  The line also carries: the same step back to back for seconds
+(``sustained``, the clock under the power cap); every other workload as the
+same fused call (``per_config``: one image, eight mixed images, the video
+batch, and the patch-16 buckets as graph replays), each with the oracle's rate
+on this host beside it; and the host-buffer path (``e2e``) with the measured
+page-locked copy bandwidth that bounds it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -189,36 +194,55 @@ def replica_value(rows_per_rank: int, world: int, ms_per_step: float) -> float:
 
 
 def run_reference(args, rank, world):
-    """The oracle timed as the reference arm: each step a strip of one image, sized so
-    the whole run stays within about two minutes."""
+    """The oracle timed as the reference arm, on this host's cores.  Each step is a bounded
+    sample of the workload (the top merge rows of one image), sized so that the whole run
+    stays within about two minutes; ms_per_step and rows_per_step are the sample's own."""
     if rank != 0:
         return 0
-    from vit_vision_encoder_fusedinputnorm_gb300 import synth
-    wl = synth.make_workload(CFG, with_pixels=False)
     per_step = max(0.2, 100.0 / (args.steps + args.warmup))
     n, dt = _oracle_strip(0, 4)                    # calibration
     merge_rows = max(1, min(48, int(4 * per_step / max(dt, 1e-3))))
     for w in range(args.warmup):
         _oracle_strip(w % 64, merge_rows)
-    rates, rows_done, t_done = [], 0, 0.0
+    rows_done, t_done = 0, 0.0
     for k in range(args.steps):
         n, dt = _oracle_strip(k % 64, merge_rows)
-        rates.append(n / dt)
         rows_done += n
         t_done += dt
     v = rows_done / t_done
-    sample = (f"each step: top {merge_rows} merge rows ({merge_rows * 2 * 96} patches) of one 1344x1344 "
-              f"image, fp64 numpy oracle")
+    strip_rows = rows_done // args.steps
+    part = "the whole image" if merge_rows >= 48 else f"its top {merge_rows} merge rows"
+    sample = (f"each step: one 1344x1344 image of the workload, {part} ({strip_rows} patches), fp64 numpy "
+              f"oracle (normalise, patchify, BLAS GEMM)")
     line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": wl.live_rows / v * 1e3, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": t_done / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
             "config": {"workload": "64 x 1344x1344 uint8 stills, patch 14, tpatch 2, merge 2, K 1176, N 1280",
-                       "rows_per_step": wl.live_rows},
+                       "rows_per_step": strip_rows,
+                       "step": "a bounded sample: one strip of one image per step (rows_per_step patches)"},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": _cores(), "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def oracle_items_rate(wl, budget_s: float):
+    """The oracle as it stands on whole items of a workload, in order, until about
+    ``budget_s`` seconds (at least one item): (patches/s, rows, items timed, seconds)."""
+    import dataclasses
+    import oracle
+    rows, t, n = 0, 0.0, 0
+    for it in wl.items:
+        sub = dataclasses.replace(wl, items=[it], bucket_rows=None, buckets=None)
+        t0 = time.perf_counter()
+        oracle.embed_workload(sub)
+        t += time.perf_counter() - t0
+        rows += it.rows
+        n += 1
+        if t >= budget_s:
+            break
+    return rows / t, rows, n, t
 
 
 def kernel_only(args):
@@ -267,6 +291,37 @@ def kernel_only(args):
     return 0
 
 
+def link_bandwidth(torch, dev, host_in, host_out, stream):
+    """Page-locked host <-> device copy bandwidth on this machine (cudaMemcpyAsync through torch):
+    up alone, down alone, and both at once on two streams.  GB/s, best of three."""
+    d_in = torch.empty(host_in.numel(), dtype=torch.uint8, device=dev)
+    d_out = torch.empty(host_out.numel() * host_out.element_size(), dtype=torch.uint8, device=dev)
+    h_out = host_out.view(-1).view(torch.uint8)
+    h_in = host_in.view(-1).view(torch.uint8)
+    s2 = torch.cuda.Stream(device=dev)
+
+    def run(up, down):
+        best = float("inf")
+        for _ in range(3):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            if up:
+                with torch.cuda.stream(stream):
+                    d_in.copy_(h_in, non_blocking=True)
+            if down:
+                with torch.cuda.stream(s2):
+                    h_out.copy_(d_out, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            best = min(best, time.perf_counter() - t0)
+        return best
+
+    t_up, t_down, t_both = run(True, False), run(False, True), run(True, True)
+    nb_in, nb_out = h_in.numel(), h_out.numel()
+    del d_in, d_out
+    return {"h2d_gbs": nb_in / t_up / 1e9, "d2h_gbs": nb_out / t_down / 1e9,
+            "both_gbs": (nb_in + nb_out) / t_both / 1e9, "both_ms": t_both * 1e3}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -274,6 +329,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--sustain-s", type=float, default=2.0,
+                    help="seconds of back-to-back steps for the sustained-clock figure (0: skip)")
+    ap.add_argument("--oracle-budget-s", type=float, default=5.0,
+                    help="seconds of oracle time per workload in the per-workload table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--datasheet", default=None,
                     help="JSON file with datasheet peaks ({\"bf16_tflops\": ..., \"hbm_gbs\": ...}); "
@@ -362,6 +421,28 @@ def main():
     embed_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     value = replica_value(rows, world, ms_step)
 
+    # the same step back to back for seconds: the clock settles where the power cap puts it
+    sustained = None
+    if args.sustain_s > 0:
+        n_sus = max(10, int(args.sustain_s / (ms_step / 1e3)))
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        smp = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+        if smp:
+            smp.start()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        s0.record(stream)
+        for _ in range(n_sus):
+            step()
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        sus_clocks = smp.stop() if smp else None
+        sus_ms = world_max(s0.elapsed_time(s1), world, dev) / n_sus
+        sustained = {"steps": n_sus, "ms_per_step": sus_ms, "patches_per_s": replica_value(rows, world, sus_ms),
+                     "clocks": sus_clocks}
+
     # end to end through the host-buffer entry point (vitfe_embed_rope_host): page-locked
     # pixels and descriptors in, embeddings and cos/sin out, the copies overlapped with the
     # launches in runs of consecutive images; wall clock around the (synchronous) call
@@ -447,50 +528,6 @@ def main():
     np_ms = looped(np_call)
     np_bytes = batch.pixel_bytes + rows * K * 2
 
-    # the patch-16 bucket workload (Qwen3-VL-like: K 1536, N 1152): one 65,536-row bucket of
-    # the varied stills, embedded with its own handle (a parity case; timed here for reference)
-    wl4 = synth.make_workload(4)
-    fe4 = FrontEnd.from_workload(wl4, device=f"cuda:{local}")
-    b4 = fe4.upload([wl4.items[i] for i in wl4.buckets[0]])
-    out4 = torch.empty((b4.live_rows, wl4.hidden), dtype=torch.bfloat16, device=dev)
-    p16_ms = timed(lambda: B.vitfe_embed(fe4.h, b4.pixels, b4.pixel_bytes, b4.items, b4.n_items, b4.capacity,
-                                         b4.live_rows, out4, None, stream))
-    p16_tflops = 2.0 * b4.live_rows * wl4.K * wl4.hidden / (p16_ms / 1e3) / 1e12
-    p16_rows = b4.live_rows
-    # ... and as the serving path runs it: one captured graph of the fused call over the fixed
-    # 65,536-row bucket (pad rows masked), replayed
-    R4 = wl4.bucket_rows
-    gout = torch.empty((R4, wl4.hidden), dtype=torch.bfloat16, device=dev)
-    gcos = torch.empty((R4, wl4.head_dim // 2), dtype=torch.float32, device=dev)
-    gsin = torch.empty_like(gcos)
-
-    def fused4():
-        B.vitfe_embed_rope(fe4.h, b4.pixels, b4.pixel_bytes, b4.items, b4.n_items, b4.capacity, R4, gout,
-                           wl4.head_dim, wl4.theta, gcos, gsin, None, stream)
-
-    with torch.cuda.stream(stream):
-        fused4()                       # builds the RoPE table outside the capture
-    torch.cuda.synchronize(dev)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        fused4()
-    p16_graph_ms = timed(graph.replay)
-    del out4, b4, gout, gcos, gsin, graph
-    fe4.close()
-
-    # the small, launch-bound workloads: one 224x224 image (256 patches) and 8 mixed images
-    # (18,048 patches), fused call latency
-    small = {}
-    for cfg_small in (0, 1):
-        wls = synth.make_workload(cfg_small)
-        fes = FrontEnd.from_workload(wls, device=f"cuda:{local}")
-        bs = fes.upload(wls.items)
-        o_s, c_s, s_s = fes.embed_rope(bs, wls.head_dim, wls.theta)
-        small[cfg_small] = (bs.live_rows, timed(lambda: B.vitfe_embed_rope(
-            fes.h, bs.pixels, bs.pixel_bytes, bs.items, bs.n_items, bs.capacity, bs.live_rows, o_s, wls.head_dim,
-            wls.theta, c_s, s_s, None, stream)))
-        fes.close()
-
     # RoPE applied to Q and K (16 + 16 heads of 80, views into a packed [rows][Q | K | V]
     # buffer), from the step's cos/sin tables: HBM bound, in place
     heads = N // wl.head_dim
@@ -505,6 +542,90 @@ def main():
     del flat
 
     pk, pk_kind = peaks()
+    burst = float(pk["bf16_tflops"])
+
+    # every other workload, as the fused call a user makes (device-resident inputs), with the
+    # oracle on this host's cores beside it
+    per_config = {}
+    cores = _cores()
+    for cfg in (0, 1, 3):
+        wlc = synth.make_workload(cfg)
+        fec = FrontEnd.from_workload(wlc, device=f"cuda:{local}")
+        bc = fec.upload(wlc.items)
+        oc, cc, sc = fec.embed_rope(bc, wlc.head_dim, wlc.theta)
+
+        def call_c():
+            B.vitfe_embed_rope(fec.h, bc.pixels, bc.pixel_bytes, bc.items, bc.n_items, bc.capacity, bc.live_rows,
+                               oc, wlc.head_dim, wlc.theta, cc, sc, None, stream)
+
+        ms_c = looped(call_c)
+        iso_c = timed(call_c)
+        fl = 2.0 * bc.live_rows * wlc.K * wlc.hidden
+        entry = {"rows": bc.live_rows, "ms": ms_c, "isolated_ms": iso_c, "patches_per_s": bc.live_rows / (ms_c / 1e3),
+                 "tflops": fl / (ms_c / 1e3) / 1e12, "frac_of_burst": fl / (ms_c / 1e3) / 1e12 / burst}
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            rate, orows, nit, ot = oracle_items_rate(wlc, args.oracle_budget_s)
+            entry["oracle"] = {"patches_per_s": rate, "cores": cores,
+                               "sample": f"{nit} of {len(wlc.items)} items, {orows} patches, {ot:.1f} s"}
+        per_config[str(cfg)] = entry
+        del oc, cc, sc
+        fec.close()
+
+    # workload 4 as the serving path runs it: one captured graph of the fused call over the
+    # fixed 65,536-row bucket, replayed once per bucket of the 50 requests
+    wl4 = synth.make_workload(4)
+    fe4 = FrontEnd.from_workload(wl4, device=f"cuda:{local}")
+    packs = [B.pack_items([wl4.items[i] for i in bk], wl4.patch, wl4.tpatch) for bk in wl4.buckets]
+    R4 = wl4.bucket_rows
+    px4 = torch.zeros(max(p[1].size for p in packs), dtype=torch.uint8, device=dev)
+    it4 = torch.zeros(B.VITFE_MAX_ITEMS * 24, dtype=torch.uint8, device=dev)
+    n4 = torch.zeros(1, dtype=torch.int32, device=dev)
+    gout = torch.empty((R4, wl4.hidden), dtype=torch.bfloat16, device=dev)
+    gcos = torch.empty((R4, wl4.head_dim // 2), dtype=torch.float32, device=dev)
+    gsin = torch.empty_like(gcos)
+
+    def fused4():
+        B.vitfe_embed_rope(fe4.h, px4, px4.numel(), it4, n4, B.VITFE_MAX_ITEMS, R4, gout, wl4.head_dim, wl4.theta,
+                           gcos, gsin, None, stream)
+
+    with torch.cuda.stream(stream):
+        fused4()                       # builds the RoPE table outside the capture
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        fused4()
+    buckets4, live4, t4 = [], 0, 0.0
+    for items, buf, live in packs:
+        px4[:buf.size].copy_(torch.from_numpy(buf))
+        arr = np.zeros(B.VITFE_MAX_ITEMS, B.ITEM_DTYPE)
+        arr[:len(items)] = items
+        it4.copy_(torch.from_numpy(arr.view(np.uint8)))
+        n4.fill_(len(items))
+        torch.cuda.synchronize(dev)
+        ms_b = looped(graph.replay, n=20, warm=3)
+        iso_b = timed(graph.replay)
+        fl = 2.0 * live * wl4.K * wl4.hidden
+        buckets4.append({"live_rows": live, "ms": ms_b, "isolated_ms": iso_b,
+                         "tflops": fl / (ms_b / 1e3) / 1e12, "frac_of_burst": fl / (ms_b / 1e3) / 1e12 / burst})
+        live4 += live
+        t4 += ms_b
+    entry4 = {"rows": live4, "bucket_rows": R4, "replays": len(packs), "ms": t4,
+              "patches_per_s": live4 / (t4 / 1e3),
+              "tflops": 2.0 * live4 * wl4.K * wl4.hidden / (t4 / 1e3) / 1e12,
+              "frac_of_burst": 2.0 * live4 * wl4.K * wl4.hidden / (t4 / 1e3) / 1e12 / burst, "buckets": buckets4}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, orows, nit, ot = oracle_items_rate(wl4, args.oracle_budget_s)
+        entry4["oracle"] = {"patches_per_s": rate, "cores": cores,
+                            "sample": f"{nit} of {len(wl4.items)} items, {orows} patches, {ot:.1f} s"}
+    per_config["4"] = entry4
+    del gout, gcos, gsin, graph, px4
+    fe4.close()
+
+    link = link_bandwidth(torch, dev, host_px, host_out, stream)
+    # the copies' floor: the download alone, the upload alone, or both directions sharing the link
+    link_floor_ms = max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9),
+                        (h2d + d2h) / (link["both_gbs"] * 1e9)) * 1e3
+
     flops = 2.0 * rows * K * N
     achieved = flops / (embed_ms / 1e3) / 1e12
     peak = float(pk["bf16_tflops"])
@@ -520,7 +641,6 @@ def main():
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(),
                      "peak_kind": f"{pk_kind} bf16 burst",
-                     "frac_of_sustained": achieved / float(pk.get("bf16_tflops_sustained", peak)),
                      "kernel": "embed_kernel<14>", "flops_per_launch": flops,
                      "kernel_ms": embed_ms},
         "datasheet": datasheet_fracs(args.datasheet, achieved, {
@@ -533,12 +653,6 @@ def main():
                                   "next (the GPU idles between them, so launch latency counts and the clock "
                                   "recovers)"),
                        "unfused_embed_then_rope_ms": unfused_ms,
-                       "patch16_bucket_embed": {"rows": p16_rows, "ms": p16_ms, "tflops": p16_tflops,
-                                                "frac_of_peak": p16_tflops / float(pk["bf16_tflops"]),
-                                                "graph_replay_embed_rope_ms": p16_graph_ms,
-                                                "bucket_rows": R4},
-                       "small_workload_embed_rope_us": {"1 x 224x224 (256 patches)": small[0][1] * 1e3,
-                                                        "8 mixed images (18,048 patches)": small[1][1] * 1e3},
                        "folded_still_variant": {"ms": folded_ms, "patches_per_s": world * rows / (folded_ms / 1e3),
                                                 "note": "approximation (W slices summed, rounded once to bf16); "
                                                         "K 588 for stills; not the method's exact result"},
@@ -556,7 +670,15 @@ def main():
                        "normalize_patchify_frac_hbm": np_bytes / (np_ms / 1e3) / 1e9 / float(pk["hbm_gbs"])},
         "e2e": {"value": world * rows / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "how": f"vitfe_embed_rope_host, page-locked host buffers, {E2E_CHUNKS} overlapped runs, wall clock"},
+                "how": f"vitfe_embed_rope_host, page-locked host buffers, {E2E_CHUNKS} overlapped runs, wall clock",
+                "link_gbs": link, "link_floor_ms": link_floor_ms, "frac_link": link_floor_ms / e2e_ms},
+        "per_config": per_config,
+        "sustained": None if sustained is None else dict(
+            sustained, tflops=flops / (sustained["ms_per_step"] / 1e3) / 1e12,
+            frac_of_sustained=flops / (sustained["ms_per_step"] / 1e3) / 1e12 / float(
+                pk.get("bf16_tflops_sustained", peak)),
+            frac_of_burst=flops / (sustained["ms_per_step"] / 1e3) / 1e12 / peak,
+            mhz_x_ms=(sustained["clocks"] or {}).get("sm_mhz", float("nan")) * sustained["ms_per_step"]),
         # per step: one embed_kernel launch that also writes the RoPE rows (the position
         # table stays cached in the handle after the first warm-up step built it)
         "gpu_launches": 1 * args.steps,
