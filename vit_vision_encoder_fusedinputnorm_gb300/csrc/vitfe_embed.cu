@@ -8,19 +8,21 @@
 //
 // Structure: persistent clusters of two CTAs (one per SM).  A pair owns 256-row tiles,
 // 128 rows per CTA; one tcgen05.mma.cta_group::2 (M=256) spans both CTAs' shared and
-// tensor memory, so each CTA holds only half of every W tile.  Per CTA, 14 warps:
-//   warps 0-7   A producers: two threads per tile row (each half of the K blocks) gather
+// tensor memory, so each CTA holds only half of every W tile.  Per CTA, 16 warps (their
+// numbers, chosen per sub-partition, are listed with the role helpers below):
+//   8 warps     A producers: two threads per tile row (each half of the K blocks) gather
 //               uint8 pixel runs with aligned 4-byte loads, normalise in fp32, round to
 //               bf16 and store into 128-byte-swizzled K-major shared-memory blocks (64
 //               features each); with patch 16 the last two blocks of each half go to
 //               tensor memory instead (tcgen05.st), and the MMA reads them from there;
-//   warp 12     TMA producer of this CTA's half of each W tile: one box copies one
-//               shared-memory image of the pre-tiled weight (bn/8 rows of 512 bytes);
-//   warp 13     tensor-memory allocation (both CTAs); in the even CTA the whole warp runs
+//   2 warps     TMA producers of this CTA's half of each W tile, alternate stages: one
+//               box copies one shared-memory image of the pre-tiled weight (bn/8 rows of
+//               512 bytes);
+//   MMA warp    tensor-memory allocation (both CTAs); in the even CTA the whole warp runs
 //               the MMA issue loop and one elected lane issues (fp32 accumulators
 //               double-buffered in tensor memory; N passes of 256 columns, or 192 with
 //               patch 16 so that the A blocks fit beside them);
-//   warps 8-11  epilogue, one warp per tensor-memory lane quarter: tcgen05.ld of the
+//   4 warps     epilogue, one warp per tensor-memory lane quarter: tcgen05.ld of the
 //               accumulator, + bias, bf16 RNE, 256-bit stores; in a vitfe_embed_rope
 //               launch also the tile's 2D-RoPE rows.
 // Barriers that gather both CTAs (A ready, W tile ready, accumulator free) live in the
@@ -45,15 +47,38 @@
 namespace vitfe {
 namespace {
 
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;            // 16 warps
 constexpr int kProducerThreads = 128;     // tile rows of a CTA (two producer threads each)
-constexpr int kProducerWarps = 8;
-constexpr int kEpilogueWarp0 = 8;
 constexpr int kEpilogueThreads = 128;     // one warp per tensor-memory lane quarter
 constexpr int kPairRows = 2 * kTileM;
-constexpr int kTmaWarp = 12;
-constexpr int kMmaWarp = 13;
+// Weight stages are loaded by two warps in turn.  With one loading warp the ring delivered
+// about 22 bytes per clock into each SM whatever its depth, below the 32 bytes per clock the
+// MMA consumes; two warps deliver the full rate.
+constexpr int kWLoaders = 2;
 constexpr int kABlockBytes = kTileM * 128;   // 128 rows x 64 bf16
+
+// Warp roles.  Warp w issues on SM sub-partition w % 4.  The producers' conversion is dense
+// ALU work, and a sub-partition shared with it slows the MMA issue loop and the weight loads
+// by about a quarter; so with patch 14 the MMA warp and both weight-loading warps sit alone on
+// sub-partition 3 (with its epilogue warp), the eight producer warps on 0-2:
+//   producers 0, 1, 2, 4 (half 0) and 5, 6, 8, 9 (half 1); MMA 3; weight loads 7, 11;
+//   epilogue 12-15 (lane quarter w % 4); warp 10 idle.
+// Patch 16's producers also write tensor memory, where warp w reaches only lane quarter
+// w % 4, so their eight warps must cover every quarter twice: producers 0-7, epilogue 8-11,
+// weight loads 12 and 14, MMA 13, warp 15 idle.
+template <int P>
+__host__ __device__ constexpr bool split_roles() { return P != 16; }   // patch 16: A blocks in tensor memory
+template <int P>
+__device__ __forceinline__ int producer_index(int w) {   // 0..7, or -1 for other roles
+  if (!split_roles<P>()) return w < 8 ? w : -1;
+  return w < 3 ? w : (w == 4 ? 3 : (w == 5 || w == 6) ? w - 1 : (w == 8 || w == 9) ? w - 2 : -1);
+}
+template <int P>
+__host__ __device__ constexpr int mma_warp() { return split_roles<P>() ? 3 : 13; }
+template <int P>
+__host__ __device__ constexpr int w_load_warp(int i) { return split_roles<P>() ? 7 + 4 * i : 12 + 2 * i; }
+template <int P>
+__host__ __device__ constexpr bool epilogue_warp(int w) { return split_roles<P>() ? w >= 12 : (w >= 8 && w < 12); }
 
 enum TileKind : int { kPad = 0, kResident = 1, kStream = 2 };
 
@@ -509,11 +534,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     build_item_table(args.items, args.n_items, args.max_items, args.pixel_bytes, P, args.T, args.M,
                      args.rows, args.rope_cos != nullptr ? VITFE_ROPE_MAX_SIDE : 0x7fffffff, tab);
   }
-  if (warp == kMmaWarp) {
+  if (warp == mma_warp<P>()) {
     tmem_alloc_pair(smem_u32(&hs->tmem_base), (uint32_t)args.tmem_cols);
     tmem_relinquish_pair();
   }
-  if (warp == kTmaWarp && lane == 0) {
+  if (warp == w_load_warp<P>(0) && lane == 0) {
     tma_prefetch_desc(&tmap_w);
     if (args.folded) tma_prefetch_desc(&tmap_wf);
   }
@@ -528,12 +553,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t acc_empty_L = mapa_shared(smem_u32(&hs->acc_empty[0]), 0);
 
   // ---- roles -------------------------------------------------------------
-  if (warp < kProducerWarps) {
+  const int pidx = producer_index<P>(warp);
+  if (pidx >= 0) {
     // A producers: this CTA's 128 rows of every pair tile, K blocks split in two halves
     const float sc[3] = {args.scale0, args.scale1, args.scale2};
     const float sh[3] = {args.shift0, args.shift1, args.shift2};
-    const int row = threadIdx.x & (kProducerThreads - 1);
-    const int half = threadIdx.x / kProducerThreads;
+    const int row = (pidx & 3) * 32 + lane;
+    const int half = pidx >> 2;
     const int rofs = (int)rank * kTileM + row;
     // this warp's lane quarter of the tensor-memory A blocks
     const uint32_t tmem_a = hs->tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
@@ -574,12 +600,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       cur = nxt;
     }
-  } else if (warp == kTmaWarp) {
+  } else if (warp == w_load_warp<P>(0) || warp == w_load_warp<P>(1)) {
     // (with the failure-detection test hook set, no weight tile is ever loaded: the MMA's
     // bounded wait runs out, every role leaves on the abort flag or its own limit)
     if (lane == 0 && !args.stall_w_loads) {
       // W tiles in consumption order: one stage per step (a step = one 64-feature K block
-      // of one temporal slice)
+      // of one temporal slice).  Both loading warps walk the whole sequence; this one
+      // issues the stages nb with nb % kWLoaders == wl.
+      const int wl = (warp == w_load_warp<P>(0)) ? 0 : 1;
       uint32_t nb = 0, stage = 0, bphase = 0;
       bool ok = true;
       for (int u = cid; ok && u < args.num_units; u += ncl) {
@@ -599,12 +627,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           return (kSharedTail && j == kNfb) ? base + Ts * kNfb : base + sl * kNfb + j;
         };
         auto load_image = [&](int img) {
-          if (!mbar_wait_cl(smem_u32(&hs->b_empty[stage]), bphase ^ 1u, abort_flag, args.limit_ns)) {
-            ok = false;
-            return;
+          if ((int)(nb % (uint32_t)kWLoaders) == wl) {
+            if (!mbar_wait_cl(smem_u32(&hs->b_empty[stage]), bphase ^ 1u, abort_flag, args.limit_ns)) {
+              ok = false;
+              return;
+            }
+            if (leader) mbar_arrive_expect_tx(smem_u32(&hs->b_full[stage]), 2u * b_stage_bytes);
+            tma_load_2d_pair(b_smem + stage * b_stage_bytes, map, b_full_L + 8u * stage, 0, img * (bnh / 4));
           }
-          if (leader) mbar_arrive_expect_tx(smem_u32(&hs->b_full[stage]), 2u * b_stage_bytes);
-          tma_load_2d_pair(b_smem + stage * b_stage_bytes, map, b_full_L + 8u * stage, 0, img * (bnh / 4));
           ++nb;
           if (++stage == (uint32_t)args.nstage) { stage = 0; bphase ^= 1u; }
         };
@@ -627,10 +657,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         if (leader) {
-          // the last loads of every stage complete on their own
+          // the last loads this warp issued complete on their own (its stages before nb were
+          // issued; nb itself was not)
           const uint32_t nlast = nb < (uint32_t)args.nstage ? nb : (uint32_t)args.nstage;
           for (uint32_t d = 1; d <= nlast; ++d) {
             const uint32_t idx = nb - d;
+            if ((int)(idx % (uint32_t)kWLoaders) != wl) continue;
             const uint32_t bar = smem_u32(&hs->b_full[idx % (uint32_t)args.nstage]);
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait_cluster(bar, (idx / (uint32_t)args.nstage) & 1u) &&
@@ -644,7 +676,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == mma_warp<P>()) {
     if (leader) {
       // The whole warp runs the issue loop, so its indices and descriptors stay warp-uniform
       // (uniform registers); one elected lane issues each group of MMAs and its commit.
@@ -817,7 +849,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
+  } else if (epilogue_warp<P>(warp)) {
     // epilogue: lane quarter q = warp % 4 of this CTA's accumulator rows
     const int q = warp & 3;
     const int rloc = (int)rank * kTileM + q * 32 + lane;
@@ -908,11 +940,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // ---- teardown ------------------------------------------------------------
   __syncwarp();
   // a producer that left on a timeout may still have tensor-memory stores in flight
-  if (ntm_blocks<P>() > 0 && warp < kProducerWarps) tmem_wait_st();
+  if (ntm_blocks<P>() > 0 && pidx >= 0) tmem_wait_st();
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc_pair(tmem, (uint32_t)args.tmem_cols);
+  if (warp == mma_warp<P>()) tmem_dealloc_pair(tmem, (uint32_t)args.tmem_cols);
   if (threadIdx.x == 0 && hs->abort_flag && args.status != nullptr) {
     args.status[0] = kTimeout;
     args.status[1] = -1;

@@ -430,9 +430,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // Bounded wait with cluster-scope acquire (barriers that peers arrive on).  Waiters off
 // the MMA-issue path pass sleep_ns > 0: after a few failed polls they back off with
 // __nanosleep so that they do not take issue slots from the warps that feed the tensor core.
-__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                             uint64_t limit_ns, uint32_t sleep_ns = 0) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
+// The first poll is inline; the polling loop is one out-of-line copy (the waits sit in fully
+// unrolled loops, and inline copies of the loop would multiply the code the SM fetches).
+static __device__ __noinline__ bool mbar_wait_cl_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               uint64_t limit_ns, uint32_t sleep_ns) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
@@ -445,6 +446,11 @@ __device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, vola
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             uint64_t limit_ns, uint32_t sleep_ns = 0) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  return mbar_wait_cl_slow(bar, parity, abort_flag, limit_ns, sleep_ns);
 }
 __device__ __forceinline__ void fence_proxy_async_all() {
   asm volatile("fence.proxy.async;" ::: "memory");
@@ -522,11 +528,11 @@ __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
   else return mbar_try_wait(bar, parity);
 }
 // sleep_ns > 0: after a few failed polls the warp backs off with __nanosleep, leaving its
-// scheduler's issue slots to the warps it shares them with.
+// scheduler's issue slots to the warps it shares them with.  As for mbar_wait_cl, the first
+// poll is inline and the loop out of line.
 template <bool kCluster>
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                               uint64_t limit_ns, uint32_t sleep_ns = 0) {
-  if (__all_sync(0xffffffffu, mbar_poll<kCluster>(bar, parity))) return true;
+static __device__ __noinline__ bool mbar_wait_warp_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                 uint64_t limit_ns, uint32_t sleep_ns) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (__all_sync(0xffffffffu, mbar_poll<kCluster>(bar, parity))) return true;
@@ -539,6 +545,12 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
       }
     }
   }
+}
+template <bool kCluster>
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               uint64_t limit_ns, uint32_t sleep_ns = 0) {
+  if (__all_sync(0xffffffffu, mbar_poll<kCluster>(bar, parity))) return true;
+  return mbar_wait_warp_slow<kCluster>(bar, parity, abort_flag, limit_ns, sleep_ns);
 }
 
 // Arrive once on the barrier at offset `bar` in both CTAs of the pair when all prior
