@@ -58,14 +58,17 @@ constexpr int kWLoaders = 2;
 constexpr int kABlockBytes = kTileM * 128;   // 128 rows x 64 bf16
 
 // Warp roles.  Warp w issues on SM sub-partition w % 4.  The producers' conversion is dense
-// ALU work, and a sub-partition shared with it slows the MMA issue loop and the weight loads
-// by about a quarter; so with patch 14 the MMA warp and both weight-loading warps sit alone on
-// sub-partition 3 (with its epilogue warp), the eight producer warps on 0-2:
-//   producers 0, 1, 2, 4 (half 0) and 5, 6, 8, 9 (half 1); MMA 3; weight loads 7, 11;
-//   epilogue 12-15 (lane quarter w % 4); warp 10 idle.
+// ALU work, and a sub-partition shared with it slows the MMA issue loop and the weight loads;
+// so with patch 14 the MMA warp sits on sub-partition 3 with one weight-loading warp and its
+// epilogue warp only, the eight producer warps on 0-2, the other loader on 2:
+//   producers 0, 1, 2, 4 (half 0) and 5, 6, 8, 9 (half 1); MMA 3; weight loads 7, 10;
+//   epilogue 12-15 (lane quarter w % 4); A-block forwarder 11.
 // Patch 16's producers also write tensor memory, where warp w reaches only lane quarter
 // w % 4, so their eight warps must cover every quarter twice: producers 0-7, epilogue 8-11,
-// weight loads 12 and 14, MMA 13, warp 15 idle.
+// weight loads 12 and 14, MMA 13, A-block forwarder 15.
+// The forwarder turns the producer warps' CTA-scope arrivals on this CTA's a_local barriers
+// into one cluster-scope arrival per block on the even CTA's a_full barrier: a cluster-scope
+// release costs about 1.4 k cycles, which the producers would otherwise pay on every block.
 template <int P>
 __host__ __device__ constexpr bool split_roles() { return P != 16; }   // patch 16: A blocks in tensor memory
 template <int P>
@@ -76,9 +79,11 @@ __device__ __forceinline__ int producer_index(int w) {   // 0..7, or -1 for othe
 template <int P>
 __host__ __device__ constexpr int mma_warp() { return split_roles<P>() ? 3 : 13; }
 template <int P>
-__host__ __device__ constexpr int w_load_warp(int i) { return split_roles<P>() ? 7 + 4 * i : 12 + 2 * i; }
+__host__ __device__ constexpr int w_load_warp(int i) { return split_roles<P>() ? (i ? 10 : 7) : 12 + 2 * i; }
 template <int P>
 __host__ __device__ constexpr bool epilogue_warp(int w) { return split_roles<P>() ? w >= 12 : (w >= 8 && w < 12); }
+template <int P>
+__host__ __device__ constexpr int forward_warp() { return split_roles<P>() ? 11 : 15; }
 
 enum TileKind : int { kPad = 0, kResident = 1, kStream = 2 };
 
@@ -114,7 +119,8 @@ struct EmbedArgs {
 
 // Shared-memory header (placed before the 1024-aligned tile area).
 struct SmemHdr {
-  uint64_t a_full[16];
+  uint64_t a_full[16];     // even CTA: block j of both CTAs is ready (one forward per CTA)
+  uint64_t a_local[16];    // this CTA's producer warps have written block j
   uint64_t a_empty[16];
   uint64_t b_full[8];
   uint64_t b_empty[8];
@@ -235,7 +241,7 @@ template <int P, int JB, int JE>
 __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, uint32_t a_smem,
                                                SmemHdr* hs, uint32_t np, int row, const float sc[3],
                                                const float sh[3], volatile int* abort_flag,
-                                               uint64_t limit_ns, uint32_t a_full_leader, uint32_t tmem_a) {
+                                               uint64_t limit_ns, uint32_t a_local0, uint32_t tmem_a) {
   constexpr int RUN = 3 * P;                 // bytes of one patch row of pixels
   constexpr int KS = 3 * P * P;
   constexpr int NBLK = (KS + 63) / 64;
@@ -351,7 +357,7 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
         if (q == 7 || kc == KEND / 8 - 1) {
           // this thread's writes become visible to the tensor core (generic-proxy shared
           // memory: proxy fence; tensor memory: wait for the stores, then the tcgen05
-          // fence); one release arrive per warp on the even CTA
+          // fence); one CTA-scope release arrive per warp on this CTA's a_local barrier
           if (in_tmem<P>(j)) {
             tmem_wait_st();
             tc_fence_before();
@@ -359,7 +365,7 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
             fence_proxy_async_smem();
           }
           __syncwarp();
-          if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(a_full_leader + 8u * (uint32_t)j);
+          if ((threadIdx.x & 31) == 0) mbar_arrive(a_local0 + 8u * (uint32_t)j);
           if (j + 1 < JE) {
             VITFE_ROWS_OF_BLOCK(j + 1);
             if (!mbar_wait_cl(a_empty0 + 8u * (uint32_t)(j + 1), empty_parity, abort_flag, limit_ns, 128))
@@ -515,7 +521,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     hs->abort_flag = 0;
     for (int j = 0; j < NBLK; ++j) {
-      mbar_init(smem_u32(&hs->a_full[j]), 2 * (kProducerThreads / 32));   // one arrive per producer warp
+      mbar_init(smem_u32(&hs->a_full[j]), 2);                          // one forward per CTA
+      mbar_init(smem_u32(&hs->a_local[j]), kProducerThreads / 32);     // one arrive per producer warp
       mbar_init(smem_u32(&hs->a_empty[j]), 1);
     }
     for (int s = 0; s < args.nstage; ++s) {
@@ -590,15 +597,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint8_t* base = cur.base0 ? cur.base0 + cur.fstride * s : nullptr;
           if (half == 0)
             ok = produce_blocks<P, 0, NBLK / 2>(base, cur.rs, a_smem, hs, np, row, sc, sh, abort_flag,
-                                                args.limit_ns, a_full_L, tmem_a);
+                                                args.limit_ns, smem_u32(&hs->a_local[0]), tmem_a);
           else
             ok = produce_blocks<P, NBLK / 2, NBLK>(base, cur.rs, a_smem, hs, np, row, sc, sh, abort_flag,
-                                                   args.limit_ns, a_full_L, tmem_a);
+                                                   args.limit_ns, smem_u32(&hs->a_local[0]), tmem_a);
           ++np;
           if (q == 0 && half == 0) prefetch_row<P>(nxt, args.T);
         }
       }
       cur = nxt;
+    }
+  } else if (warp == forward_warp<P>()) {
+    // every production of this CTA's A blocks, block by block in the order the MMA consumes
+    // them: wait for the producer warps' local arrivals, then one cluster-scope arrival on
+    // the even CTA's a_full barrier
+    uint32_t np = 0;
+    bool ok = true;
+    const uint32_t a_local0 = smem_u32(&hs->a_local[0]);
+    for (int u = cid; ok && u < args.num_units; u += ncl) {
+      int tile, p_lo, p_hi;
+      unit_range(args, u, tile, p_lo, p_hi);
+      const int kind = tile_kind(tile * kPairRows, hs, args.T);
+      if (kind == kPad) continue;
+      const int nprod = (kind == kResident) ? 1 : ((p_hi - p_lo + 1) / 2) * args.T;
+      for (int q = 0; ok && q < nprod; ++q) {
+#pragma unroll 1
+        for (int jj = 0; jj < NBLK; ++jj) {
+          const int j = blk_order<NBLK>(jj);
+          if (!mbar_wait_warp<false>(a_local0 + 8u * (uint32_t)j, np & 1u, abort_flag, args.limit_ns, 32)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_cluster(a_full_L + 8u * (uint32_t)j);
+          __syncwarp();
+        }
+        ++np;
+      }
     }
   } else if (warp == w_load_warp<P>(0) || warp == w_load_warp<P>(1)) {
     // (with the failure-detection test hook set, no weight tile is ever loaded: the MMA's
