@@ -493,6 +493,11 @@ __device__ __forceinline__ void prefetch_row(const RowSrc& src, int nslices) {
   }
 }
 
+// the first pass's wait for a fresh A block, out of line (once per block and tile)
+__device__ __noinline__ bool wait_a_block(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns) {
+  return mbar_wait_warp<true>(bar, parity, abort_flag, limit_ns);
+}
+
 template <int P>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     embed_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_wf,
@@ -815,7 +820,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < NBLK; ++jj) {
               const int j = blk_order<NBLK>(jj);
-              if (p == p_lo) VITFE_WAIT_A(j);   // the unit's first pass meets the fresh A
+              if (p == p_lo) {   // the unit's first pass meets the fresh A
+                if (!wait_a_block(a_full0 + 8u * (uint32_t)j, np & 1u, abort_flag, args.limit_ns)) ok = false;
+                if (in_tmem<P>(j)) tc_fence_after();
+              }
               const uint64_t ad = adesc0 + (uint64_t)(smem_slot<P>(j) * (kABlockBytes >> 4));
               if (kSharedTail && j == kNfb) {
                 VITFE_WAIT_B();
