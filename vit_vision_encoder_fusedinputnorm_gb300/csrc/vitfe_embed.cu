@@ -232,11 +232,13 @@ __device__ __forceinline__ uint64_t norm2(uint64_t v, uint64_t scale2, uint64_t 
 // hide each other's load latency.
 //
 // Schedule per K block j: convert and store its 64 features, make them visible to the
-// tensor core (proxy fence + release arrive on the even CTA's barrier), then issue the
-// loads of the patch rows that start in block j+1 and wait for block j+1's shared-memory
-// slot to be freed.  Every load is consumed inside the block it starts in, so no load is
-// in flight when the release arrive executes (a release waits for the thread's pending
-// loads); the load latency overlaps the wait for the free slot.
+// tensor core (proxy fence + CTA-scope release arrive on this CTA's a_local barrier, which
+// the forwarder warp passes on), then wait for block j+1's shared-memory slot to be freed.
+// The pixel rows are loaded two rows ahead (row r+2 as soon as row r has been realigned),
+// so a row's load latency overlaps the conversion of the row before it; a load may then
+// still be in flight at a release arrive, which waits for it, but it was issued a row's
+// conversion earlier (before, the loads of block j+1 were issued after block j's arrive and
+// their whole latency came before block j+1's conversion).
 template <int P, int JB, int JE>
 __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, uint32_t a_smem,
                                                SmemHdr* hs, uint32_t np, int row, const float sc[3],
@@ -252,13 +254,9 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
   constexpr int E1 = (64 * JE < KEND) ? 64 * JE : KEND;   // one past the last feature written
   constexpr int R0 = E0 / RUN;               // first pixel row touched
   constexpr int RL = ((E1 < KS ? E1 : KS) - 1) / RUN;      // last pixel row touched
-  // Register ring of loaded pixel rows: row r+2 is loaded at the end of a block that
-  // comes after row r started (2*RUN > 64), so two slots suffice -- except at the start of
-  // a range that begins inside row R0, where row R0+2 may also start in block JB: its load
-  // is deferred until row R0 has been aligned (DEFER).
+  // Register ring of loaded pixel rows: row r+2 goes into row r's slot right after row r
+  // has been realigned into al[], so two slots suffice.
   constexpr int R = 2;
-  constexpr bool CARRY = (R0 * RUN < E0) && R0 < P;            // R0 started before the range
-  constexpr bool DEFER = CARRY && (R0 + 2 < P) && ((R0 + 2) * RUN < 64 * (JB + 1));
   static_assert(RUN % 2 == 0 && RUN > 32, "patch rows: even length, at most two start per block");
   static_assert(NBLK <= 16 && JB < JE && JE <= NBLK, "A slots");
   // (scale, shift) of the channel pairs (c, c+1 mod 3) that a feature pair starting at
@@ -286,24 +284,12 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
         raw[(PH) % R][w_] = (4u * w_ < s_ + RUN) ? __ldg(w0_ + w_) : 0u;                     \
     }                                                                                        \
   } while (0)
-  // Rows starting in block b: [ceil(64b/RUN), ceil(64(b+1)/RUN)); at most two.
-#define VITFE_ROWS_OF_BLOCK(B)                                                    \
-  do {                                                                             \
-    const int lo_ = (64 * (B) + RUN - 1) / RUN;                                    \
-    const int hi_ = (64 * ((B) + 1) + RUN - 1) / RUN;                              \
-    if (lo_ < hi_ && lo_ < P) VITFE_LOAD_ROW(lo_);                                 \
-    if (lo_ + 1 < hi_ && lo_ + 1 < P) VITFE_LOAD_ROW(lo_ + 1);                     \
-  } while (0)
-
-  // first block: the row it starts inside (if a row began in an earlier block), the rows
-  // that start in it, then its slot
-  if (CARRY) VITFE_LOAD_ROW(R0);
-  {
-    const int lo_ = (64 * JB + RUN - 1) / RUN;
-    const int hi_ = (64 * (JB + 1) + RUN - 1) / RUN;
-    if (lo_ < hi_ && lo_ < P && !(DEFER && lo_ == R0 + 2)) VITFE_LOAD_ROW(lo_);
-    if (lo_ + 1 < hi_ && lo_ + 1 < P && !(DEFER && lo_ + 1 == R0 + 2)) VITFE_LOAD_ROW(lo_ + 1);
-  }
+  // the range's first two rows (the first may have started in an earlier block), then the
+  // first block's slot; every later row is loaded two rows ahead, as soon as the row that
+  // held its register slot has been realigned, so that its latency overlaps the conversion
+  // of the row in between
+  VITFE_LOAD_ROW(R0);
+  if (R0 + 1 <= RL && R0 + 1 < P) VITFE_LOAD_ROW(R0 + 1);
   if (!mbar_wait_cl(a_empty0 + 8u * JB, empty_parity, abort_flag, limit_ns, 128)) return false;
   if (in_tmem<P>(JB)) tc_fence_after();
 
@@ -317,7 +303,7 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
       const uint32_t sl = 0x3210u + 0x1111u * (uint32_t)(reinterpret_cast<uintptr_t>(base + (int64_t)ph * rs) & 3u);
 #pragma unroll
       for (int w = 0; w < NA; ++w) al[w] = __byte_perm(raw[ph % R][w], raw[ph % R][w + 1], sl);
-      if (DEFER && ph == R0) VITFE_LOAD_ROW(R0 + 2);
+      if (ph + 2 <= RL && ph + 2 < P) VITFE_LOAD_ROW(ph + 2);
     } else {
 #pragma unroll
       for (int w = 0; w < NA; ++w) al[w] = 0u;
@@ -367,7 +353,6 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
           __syncwarp();
           if ((threadIdx.x & 31) == 0) mbar_arrive(a_local0 + 8u * (uint32_t)j);
           if (j + 1 < JE) {
-            VITFE_ROWS_OF_BLOCK(j + 1);
             if (!mbar_wait_cl(a_empty0 + 8u * (uint32_t)(j + 1), empty_parity, abort_flag, limit_ns, 128))
               return false;
             if (in_tmem<P>(j + 1)) tc_fence_after();
@@ -376,7 +361,6 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
       }
     }
   }
-#undef VITFE_ROWS_OF_BLOCK
 #undef VITFE_LOAD_ROW
   return true;
 }
