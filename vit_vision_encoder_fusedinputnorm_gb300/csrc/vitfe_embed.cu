@@ -62,13 +62,16 @@ constexpr int kABlockBytes = kTileM * 128;   // 128 rows x 64 bf16
 // so with patch 14 the MMA warp sits on sub-partition 3 with one weight-loading warp and its
 // epilogue warp only, the eight producer warps on 0-2, the other loader on 2:
 //   producers 0, 1, 2, 4 (half 0) and 5, 6, 8, 9 (half 1); MMA 3; weight loads 7, 10;
-//   epilogue 12-15 (lane quarter w % 4); A-block forwarder 11.
+//   epilogue 12-15 (lane quarter w % 4); A-block forwarder 11 (odd CTA; idle in the even).
 // Patch 16's producers also write tensor memory, where warp w reaches only lane quarter
 // w % 4, so their eight warps must cover every quarter twice: producers 0-7, epilogue 8-11,
 // weight loads 12 and 14, MMA 13, A-block forwarder 15.
-// The forwarder turns the producer warps' CTA-scope arrivals on this CTA's a_local barriers
-// into one cluster-scope arrival per block on the even CTA's a_full barrier: a cluster-scope
-// release costs about 1.4 k cycles, which the producers would otherwise pay on every block.
+// A cluster-scope release costs about 1.4 k cycles, which producer warps arriving on the
+// even CTA's barrier would pay on every block.  So the even CTA's producers arrive with
+// CTA scope on its a_full barriers directly, and the odd CTA's arrive with CTA scope on
+// their own a_local barriers; the odd CTA's forwarder passes those on to the even CTA two
+// blocks at a time, in the MMA's consumption order: one release, which the MMA acquires
+// with the first of the two blocks, then a relaxed arrival for the second.
 template <int P>
 __host__ __device__ constexpr bool split_roles() { return P != 16; }   // patch 16: A blocks in tensor memory
 template <int P>
@@ -119,8 +122,9 @@ struct EmbedArgs {
 
 // Shared-memory header (placed before the 1024-aligned tile area).
 struct SmemHdr {
-  uint64_t a_full[16];     // even CTA: block j of both CTAs is ready (one forward per CTA)
-  uint64_t a_local[16];    // this CTA's producer warps have written block j
+  uint64_t a_full[16];     // even CTA: block j of both CTAs is ready (its own producer warps
+                           // and one forward from the odd CTA)
+  uint64_t a_local[16];    // odd CTA: this CTA's producer warps have written block j
   uint64_t a_empty[16];
   uint64_t b_full[8];
   uint64_t b_empty[8];
@@ -343,7 +347,8 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
         if (q == 7 || kc == KEND / 8 - 1) {
           // this thread's writes become visible to the tensor core (generic-proxy shared
           // memory: proxy fence; tensor memory: wait for the stores, then the tcgen05
-          // fence); one CTA-scope release arrive per warp on this CTA's a_local barrier
+          // fence); one CTA-scope release arrive per warp: on a_full in the even CTA, on
+          // a_local in the odd one (passed on by its forwarder)
           if (in_tmem<P>(j)) {
             tmem_wait_st();
             tc_fence_before();
@@ -510,7 +515,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     hs->abort_flag = 0;
     for (int j = 0; j < NBLK; ++j) {
-      mbar_init(smem_u32(&hs->a_full[j]), 2);                          // one forward per CTA
+      mbar_init(smem_u32(&hs->a_full[j]), kProducerThreads / 32 + 1);  // even CTA's warps + the odd CTA
       mbar_init(smem_u32(&hs->a_local[j]), kProducerThreads / 32);     // one arrive per producer warp
       mbar_init(smem_u32(&hs->a_empty[j]), 1);
     }
@@ -559,6 +564,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int rofs = (int)rank * kTileM + row;
     // this warp's lane quarter of the tensor-memory A blocks
     const uint32_t tmem_a = hs->tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
+    // block-ready barriers this CTA's producer warps arrive on
+    const uint32_t a_ready0 = leader ? smem_u32(&hs->a_full[0]) : smem_u32(&hs->a_local[0]);
     uint32_t np = 0;
     bool ok = true;
     int u = cid;
@@ -586,20 +593,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint8_t* base = cur.base0 ? cur.base0 + cur.fstride * s : nullptr;
           if (half == 0)
             ok = produce_blocks<P, 0, NBLK / 2>(base, cur.rs, a_smem, hs, np, row, sc, sh, abort_flag,
-                                                args.limit_ns, smem_u32(&hs->a_local[0]), tmem_a);
+                                                args.limit_ns, a_ready0, tmem_a);
           else
             ok = produce_blocks<P, NBLK / 2, NBLK>(base, cur.rs, a_smem, hs, np, row, sc, sh, abort_flag,
-                                                   args.limit_ns, smem_u32(&hs->a_local[0]), tmem_a);
+                                                   args.limit_ns, a_ready0, tmem_a);
           ++np;
           if (q == 0 && half == 0) prefetch_row<P>(nxt, args.T);
         }
       }
       cur = nxt;
     }
-  } else if (warp == forward_warp<P>()) {
-    // every production of this CTA's A blocks, block by block in the order the MMA consumes
-    // them: wait for the producer warps' local arrivals, then one cluster-scope arrival on
-    // the even CTA's a_full barrier
+  } else if (warp == forward_warp<P>() && !leader) {
+    // every production of this CTA's A blocks, two blocks at a time in the order the MMA
+    // consumes them: wait for the producer warps' local arrivals on both, then one
+    // cluster-scope release arrival for the first and a relaxed one for the second (the MMA
+    // acquires the first block's barrier before it waits for the second's)
     uint32_t np = 0;
     bool ok = true;
     const uint32_t a_local0 = smem_u32(&hs->a_local[0]);
@@ -610,14 +618,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (kind == kPad) continue;
       const int nprod = (kind == kResident) ? 1 : ((p_hi - p_lo + 1) / 2) * args.T;
       for (int q = 0; ok && q < nprod; ++q) {
+        static_assert(NBLK % 2 == 0, "blocks forwarded in pairs");
 #pragma unroll 1
-        for (int jj = 0; jj < NBLK; ++jj) {
-          const int j = blk_order<NBLK>(jj);
-          if (!mbar_wait_warp<false>(a_local0 + 8u * (uint32_t)j, np & 1u, abort_flag, args.limit_ns, 32)) {
+        for (int jj = 0; jj < NBLK; jj += 2) {
+          const int j0 = blk_order<NBLK>(jj), j1 = blk_order<NBLK>(jj + 1);
+          if (!mbar_wait_warp<false>(a_local0 + 8u * (uint32_t)j0, np & 1u, abort_flag, args.limit_ns, 32) ||
+              !mbar_wait_warp<false>(a_local0 + 8u * (uint32_t)j1, np & 1u, abort_flag, args.limit_ns, 32)) {
             ok = false;
             break;
           }
-          if (lane == 0) mbar_arrive_cluster(a_full_L + 8u * (uint32_t)j);
+          if (lane == 0) {
+            mbar_arrive_cluster(a_full_L + 8u * (uint32_t)j0);
+            mbar_arrive_cluster_relaxed(a_full_L + 8u * (uint32_t)j1);
+          }
           __syncwarp();
         }
         ++np;
