@@ -465,21 +465,10 @@ __device__ __forceinline__ RowSrc row_src(const EmbedArgs& args, const SmemHdr* 
   return src;
 }
 
-// Pull the pixel runs of a row into L2 ahead of its production (first and last byte of
-// every run of every slice the row reads).
-template <int P>
-__device__ __forceinline__ void prefetch_row(const RowSrc& src, int nslices) {
-  if (src.base0 == nullptr) return;
-  for (int sl = 0; sl < nslices; ++sl) {
-    const uint8_t* b = src.base0 + src.fstride * sl;
-#pragma unroll
-    for (int ph = 0; ph < P; ++ph) {
-      const uint8_t* a = b + (int64_t)ph * src.rs;
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(a + 3 * P - 1));
-    }
-    if (src.fstride == 0) break;
-  }
+// the MMA's elected lane's wait for a weight stage that had not landed at the first poll,
+// out of line
+__device__ __noinline__ bool wait_w_stage(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns) {
+  return mbar_wait(bar, parity, abort_flag, limit_ns);
 }
 
 // the first pass's wait for a fresh A block, out of line (once per block and tile)
@@ -576,7 +565,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     };
     RowSrc cur = u < args.num_units ? row_src<P>(args, hs, tile_of(u) * kPairRows + rofs)
                                     : RowSrc{nullptr, 0, 0};
-    if (half == 0) prefetch_row<P>(cur, args.T);
     for (; ok && u < args.num_units; u += ncl) {
       int tile, p_lo, p_hi;
       unit_range(args, u, tile, p_lo, p_hi);
@@ -598,7 +586,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = produce_blocks<P, NBLK / 2, NBLK>(base, cur.rs, a_smem, hs, np, row, sc, sh, abort_flag,
                                                    args.limit_ns, a_ready0, tmem_a);
           ++np;
-          if (q == 0 && half == 0) prefetch_row<P>(nxt, args.T);
         }
       }
       cur = nxt;
@@ -732,37 +719,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t nstage = (uint32_t)args.nstage;
       const int T = args.T;
 
-#define VITFE_WAIT_B()                                                                        \
-  do {                                                                                        \
-    if (!mbar_wait_warp<false>(b_full0 + 8u * stage, bphase, abort_flag, args.limit_ns)) ok = false; \
-  } while (0)
 #define VITFE_WAIT_A(J)                                                                       \
   do {                                                                                        \
     if (!mbar_wait_warp<true>(a_full0 + 8u * (J), np & 1u, abort_flag, args.limit_ns)) ok = false; \
     if (in_tmem<P>(J)) tc_fence_after();                                                      \
   } while (0)
-// one stage: the K16 MMAs of block J (A in shared memory at descriptor ADESC, or in
-// tensor memory) against the stage's W image from K16 step BOFF / 2 on, then the stage's
-// release
+// One stage: the elected lane waits for the stage's W image (the poll and, when it is not
+// there yet, the bounded wait out of line), then issues the K16 MMAs of block J (A in shared
+// memory at descriptor ADESC, or in tensor memory) against the image from K16 step BOFF / 2
+// on, and the stage's release.  One vote ends the stage: it carries a timed-out wait to every
+// lane and reconverges the warp (a warp-wide poll and vote before the MMAs cost more issue
+// time per stage).
 #define VITFE_STEP(D, ID, J, ADESC, NK, FIRST, BOFF)                                          \
   do {                                                                                        \
     const uint64_t bd_ = bd_cur + (uint64_t)(BOFF);                                           \
+    bool go_ = true;                                                                          \
     if (elect_one()) {                                                                        \
-      if (in_tmem<P>(J)) {                                                                    \
-        const uint32_t ta_ = tmem + tm_col<P>(J);                                             \
-        umma_bf16_pair_ta((D), ta_, bd_, (ID), (FIRST) ? 0u : 1u);                            \
-        if ((NK) > 1) umma_bf16_pair_ta((D), ta_ + 8u, bd_ + 2u, (ID), 1u);                  \
-        if ((NK) > 2) umma_bf16_pair_ta((D), ta_ + 16u, bd_ + 4u, (ID), 1u);                 \
-        if ((NK) > 3) umma_bf16_pair_ta((D), ta_ + 24u, bd_ + 6u, (ID), 1u);                 \
-      } else {                                                                                \
-        umma_bf16_pair((D), (ADESC), bd_, (ID), (FIRST) ? 0u : 1u);                           \
-        if ((NK) > 1) umma_bf16_pair((D), (ADESC) + 2u, bd_ + 2u, (ID), 1u);                 \
-        if ((NK) > 2) umma_bf16_pair((D), (ADESC) + 4u, bd_ + 4u, (ID), 1u);                 \
-        if ((NK) > 3) umma_bf16_pair((D), (ADESC) + 6u, bd_ + 6u, (ID), 1u);                 \
+      go_ = mbar_try_wait(b_full0 + 8u * stage, bphase) ||                                    \
+            wait_w_stage(b_full0 + 8u * stage, bphase, abort_flag, args.limit_ns);            \
+      if (go_) {                                                                              \
+        if (in_tmem<P>(J)) {                                                                  \
+          const uint32_t ta_ = tmem + tm_col<P>(J);                                           \
+          umma_bf16_pair_ta((D), ta_, bd_, (ID), (FIRST) ? 0u : 1u);                          \
+          if ((NK) > 1) umma_bf16_pair_ta((D), ta_ + 8u, bd_ + 2u, (ID), 1u);                \
+          if ((NK) > 2) umma_bf16_pair_ta((D), ta_ + 16u, bd_ + 4u, (ID), 1u);               \
+          if ((NK) > 3) umma_bf16_pair_ta((D), ta_ + 24u, bd_ + 6u, (ID), 1u);               \
+        } else {                                                                              \
+          umma_bf16_pair((D), (ADESC), bd_, (ID), (FIRST) ? 0u : 1u);                         \
+          if ((NK) > 1) umma_bf16_pair((D), (ADESC) + 2u, bd_ + 2u, (ID), 1u);               \
+          if ((NK) > 2) umma_bf16_pair((D), (ADESC) + 4u, bd_ + 4u, (ID), 1u);               \
+          if ((NK) > 3) umma_bf16_pair((D), (ADESC) + 6u, bd_ + 6u, (ID), 1u);               \
+        }                                                                                     \
+        umma_commit_pair(b_empty0 + 8u * stage);                                              \
       }                                                                                       \
-      umma_commit_pair(b_empty0 + 8u * stage);                                                \
     }                                                                                         \
-    __syncwarp();                                                                             \
+    if (!__all_sync(0xffffffffu, go_)) ok = false;                                            \
     if (++stage == nstage) {                                                                  \
       stage = 0;                                                                              \
       bphase ^= 1u;                                                                           \
@@ -777,11 +768,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #define VITFE_STEP_TAILS(D, ID, ADESC, NS)                                                    \
   do {                                                                                        \
     const uint64_t bd_ = bd_cur;                                                              \
+    bool go_ = true;                                                                          \
     if (elect_one()) {                                                                        \
-      for (int s_ = 0; s_ < (NS); ++s_) umma_bf16_pair((D), (ADESC), bd_ + 2u * (uint64_t)s_, (ID), 1u); \
-      umma_commit_pair(b_empty0 + 8u * stage);                                                \
+      go_ = mbar_try_wait(b_full0 + 8u * stage, bphase) ||                                    \
+            wait_w_stage(b_full0 + 8u * stage, bphase, abort_flag, args.limit_ns);            \
+      if (go_) {                                                                              \
+        for (int s_ = 0; s_ < (NS); ++s_) umma_bf16_pair((D), (ADESC), bd_ + 2u * (uint64_t)s_, (ID), 1u); \
+        umma_commit_pair(b_empty0 + 8u * stage);                                              \
+      }                                                                                       \
     }                                                                                         \
-    __syncwarp();                                                                             \
+    if (!__all_sync(0xffffffffu, go_)) ok = false;                                            \
     if (++stage == nstage) {                                                                  \
       stage = 0;                                                                              \
       bphase ^= 1u;                                                                           \
@@ -821,17 +817,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!wait_a_block(a_full0 + 8u * (uint32_t)j, np & 1u, abort_flag, args.limit_ns)) ok = false;
                 if (in_tmem<P>(j)) tc_fence_after();
               }
+              if (!ok) break;
               const uint64_t ad = adesc0 + (uint64_t)(smem_slot<P>(j) * (kABlockBytes >> 4));
               if (kSharedTail && j == kNfb) {
-                VITFE_WAIT_B();
-                if (!ok) break;
                 VITFE_STEP_TAILS(d_tmem, idesc, ad, Ts);
               } else {
-                for (int sl = 0; ok && sl < Ts; ++sl) {
-                  VITFE_WAIT_B();
-                  if (!ok) break;
+                for (int sl = 0; ok && sl < Ts; ++sl)
                   VITFE_STEP(d_tmem, idesc, j, ad, ksteps_of<P>(j), j == 0 && sl == 0, 0u);
-                }
               }
               if (!ok) break;
               if (p == p_hi - 1) {
@@ -852,9 +844,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // one copy of the issue code for both passes (code size: the issue loop is
                 // sensitive to instruction fetch)
 #pragma unroll 1
-                for (int g = 0; g < G; ++g) {
-                  VITFE_WAIT_B();
-                  if (!ok) break;
+                for (int g = 0; ok && g < G; ++g) {
                   VITFE_STEP(g ? d_tmem1 : d_tmem, g ? idesc1 : idesc, j, ad, ksteps_of<P>(j), sl == 0 && j == 0,
                              (kSharedTail && j == kNfb) ? 2u * (uint32_t)sl : 0u);
                 }
@@ -878,7 +868,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #undef VITFE_STEP_TAILS
 #undef VITFE_STEP
 #undef VITFE_WAIT_A
-#undef VITFE_WAIT_B
       if (!ok) {
         // the elected lane issued every MMA: its commit covers them all
         if (elect_one()) umma_commit_pair(smem_u32(&hs->drain));
