@@ -294,7 +294,7 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
   // of the row in between
   VITFE_LOAD_ROW(R0);
   if (R0 + 1 <= RL && R0 + 1 < P) VITFE_LOAD_ROW(R0 + 1);
-  if (!mbar_wait_cl(a_empty0 + 8u * JB, empty_parity, abort_flag, limit_ns, 128)) return false;
+  if (!mbar_wait_cl(a_empty0 + 8u * JB, empty_parity, abort_flag, limit_ns, 32)) return false;
   if (in_tmem<P>(JB)) tc_fence_after();
 
 #pragma unroll
@@ -358,7 +358,7 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
           __syncwarp();
           if ((threadIdx.x & 31) == 0) mbar_arrive(a_local0 + 8u * (uint32_t)j);
           if (j + 1 < JE) {
-            if (!mbar_wait_cl(a_empty0 + 8u * (uint32_t)(j + 1), empty_parity, abort_flag, limit_ns, 128))
+            if (!mbar_wait_cl(a_empty0 + 8u * (uint32_t)(j + 1), empty_parity, abort_flag, limit_ns, 32))
               return false;
             if (in_tmem<P>(j + 1)) tc_fence_after();
           }
@@ -471,7 +471,13 @@ __device__ __noinline__ bool wait_w_stage(uint32_t bar, uint32_t parity, volatil
   return mbar_wait(bar, parity, abort_flag, limit_ns);
 }
 
-// the first pass's wait for a fresh A block, out of line (once per block and tile)
+// the MMA's elected lane's wait for a fresh A block that was not ready at the first poll
+// (cluster-scope acquire: the odd CTA's blocks are published from there), out of line
+__device__ __noinline__ bool wait_a_lane(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns) {
+  return mbar_wait_cl_slow(bar, parity, abort_flag, limit_ns, 0u);
+}
+
+// the first pass's warp-wide wait for a fresh A block, out of line (once per block and tile)
 __device__ __noinline__ bool wait_a_block(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns) {
   return mbar_wait_warp<true>(bar, parity, abort_flag, limit_ns);
 }
@@ -483,6 +489,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   constexpr int NBLK = nblk_of<P>();
   constexpr bool kSharedTail = w_tail_shared(3 * P * P);         // the slices' tails share an image
   constexpr int kNfb = kSharedTail ? (3 * P * P) / 64 : NBLK;    // blocks with one image per slice
+  constexpr bool kLaneAWait = split_roles<P>();                  // first-pass A waits in the issuing lane
   extern __shared__ uint8_t smem_raw[];
   SmemHdr* hs = reinterpret_cast<SmemHdr*>(smem_raw);
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -724,19 +731,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (!mbar_wait_warp<true>(a_full0 + 8u * (J), np & 1u, abort_flag, args.limit_ns)) ok = false; \
     if (in_tmem<P>(J)) tc_fence_after();                                                      \
   } while (0)
-// One stage: the elected lane waits for the stage's W image (the poll and, when it is not
-// there yet, the bounded wait out of line), then issues the K16 MMAs of block J (A in shared
-// memory at descriptor ADESC, or in tensor memory) against the image from K16 step BOFF / 2
-// on, and the stage's release.  One vote ends the stage: it carries a timed-out wait to every
-// lane and reconverges the warp (a warp-wide poll and vote before the MMAs cost more issue
-// time per stage).
-#define VITFE_STEP(D, ID, J, ADESC, NK, FIRST, BOFF)                                          \
+// One stage, issued by the elected lane alone: with AW it first waits for A block J (the
+// producers' release, cluster-scope acquire); then it waits for the stage's W image (one
+// poll; when the image has not landed, the bounded wait out of line), issues the K16 MMAs of
+// block J (A in shared memory at descriptor ADESC, or in tensor memory) against the image
+// from K16 step BOFF / 2 on, and the stage's release.  One vote ends the stage: it carries a
+// timed-out wait to every lane and reconverges the warp (warp-wide polls and votes before
+// the MMAs cost more issue time per stage).
+#define VITFE_STEP(D, ID, J, ADESC, NK, FIRST, BOFF, AW)                                      \
   do {                                                                                        \
     const uint64_t bd_ = bd_cur + (uint64_t)(BOFF);                                           \
     bool go_ = true;                                                                          \
     if (elect_one()) {                                                                        \
-      go_ = mbar_try_wait(b_full0 + 8u * stage, bphase) ||                                    \
-            wait_w_stage(b_full0 + 8u * stage, bphase, abort_flag, args.limit_ns);            \
+      if (AW) {                                                                               \
+        go_ = mbar_try_wait_cluster(a_full0 + 8u * (J), np & 1u) ||                           \
+              wait_a_lane(a_full0 + 8u * (J), np & 1u, abort_flag, args.limit_ns);            \
+        if (in_tmem<P>(J)) tc_fence_after();                                                  \
+      }                                                                                       \
+      go_ = go_ && (mbar_try_wait(b_full0 + 8u * stage, bphase) ||                            \
+                    wait_w_stage(b_full0 + 8u * stage, bphase, abort_flag, args.limit_ns));   \
       if (go_) {                                                                              \
         if (in_tmem<P>(J)) {                                                                  \
           const uint32_t ta_ = tmem + tm_col<P>(J);                                           \
@@ -763,15 +776,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }                                                                                         \
   } while (0)
 
-// one stage holding the NS temporal slices' one-step tails: each slice's K16 MMA against
-// the same A block, slice s at K16 step s of the image (never a pass's first MMA)
-#define VITFE_STEP_TAILS(D, ID, ADESC, NS)                                                    \
+// one stage holding the NS temporal slices' one-step tails of block kNfb: each slice's K16
+// MMA against the same A block, slice s at K16 step s of the image (never a pass's first
+// MMA); AW as for VITFE_STEP
+#define VITFE_STEP_TAILS(D, ID, ADESC, NS, AW)                                                \
   do {                                                                                        \
     const uint64_t bd_ = bd_cur;                                                              \
     bool go_ = true;                                                                          \
     if (elect_one()) {                                                                        \
-      go_ = mbar_try_wait(b_full0 + 8u * stage, bphase) ||                                    \
-            wait_w_stage(b_full0 + 8u * stage, bphase, abort_flag, args.limit_ns);            \
+      if (AW) {                                                                               \
+        go_ = mbar_try_wait_cluster(a_full0 + 8u * kNfb, np & 1u) ||                          \
+              wait_a_lane(a_full0 + 8u * kNfb, np & 1u, abort_flag, args.limit_ns);           \
+        if (in_tmem<P>(kNfb)) tc_fence_after();                                               \
+      }                                                                                       \
+      go_ = go_ && (mbar_try_wait(b_full0 + 8u * stage, bphase) ||                            \
+                    wait_w_stage(b_full0 + 8u * stage, bphase, abort_flag, args.limit_ns));   \
       if (go_) {                                                                              \
         for (int s_ = 0; s_ < (NS); ++s_) umma_bf16_pair((D), (ADESC), bd_ + 2u * (uint64_t)s_, (ID), 1u); \
         umma_commit_pair(b_empty0 + 8u * stage);                                              \
@@ -813,17 +832,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < NBLK; ++jj) {
               const int j = blk_order<NBLK>(jj);
-              if (p == p_lo) {   // the unit's first pass meets the fresh A
+              // the unit's first pass meets the fresh A: each block is waited for before its
+              // first stage, by the issuing lane (patch 14) or by the whole warp (patch 16, where
+              // the lane's wait measured slower)
+              if (!kLaneAWait && p == p_lo) {
                 if (!wait_a_block(a_full0 + 8u * (uint32_t)j, np & 1u, abort_flag, args.limit_ns)) ok = false;
                 if (in_tmem<P>(j)) tc_fence_after();
               }
               if (!ok) break;
+              const bool aw = kLaneAWait && p == p_lo;
               const uint64_t ad = adesc0 + (uint64_t)(smem_slot<P>(j) * (kABlockBytes >> 4));
               if (kSharedTail && j == kNfb) {
-                VITFE_STEP_TAILS(d_tmem, idesc, ad, Ts);
+                VITFE_STEP_TAILS(d_tmem, idesc, ad, Ts, aw);
               } else {
                 for (int sl = 0; ok && sl < Ts; ++sl)
-                  VITFE_STEP(d_tmem, idesc, j, ad, ksteps_of<P>(j), j == 0 && sl == 0, 0u);
+                  VITFE_STEP(d_tmem, idesc, j, ad, ksteps_of<P>(j), j == 0 && sl == 0, 0u, aw && sl == 0);
               }
               if (!ok) break;
               if (p == p_hi - 1) {
@@ -846,7 +869,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                 for (int g = 0; ok && g < G; ++g) {
                   VITFE_STEP(g ? d_tmem1 : d_tmem, g ? idesc1 : idesc, j, ad, ksteps_of<P>(j), sl == 0 && j == 0,
-                             (kSharedTail && j == kNfb) ? 2u * (uint32_t)sl : 0u);
+                             (kSharedTail && j == kNfb) ? 2u * (uint32_t)sl : 0u, false);
                 }
                 if (!ok) break;
                 if (elect_one()) umma_commit_pair(a_empty0 + 8u * j);
