@@ -465,6 +465,45 @@ def test_embed_rope_one_launch_equals_the_two_calls(name):
     fe.close()
 
 
+def test_back_to_back_calls_into_one_buffer_keep_stream_order():
+    # Consecutive fused calls on one stream may overlap (the next call's prologue, A
+    # production and first passes run while the previous call finishes); every global write
+    # of a call still lands after the previous call's.  A chain A, B, A, B ... into the same
+    # outputs must leave exactly B's result, and a torch read between two calls must see the
+    # first call's result.
+    import torch
+    wa = synth.small_workload(61, [(1, 16, 16, 1), (2, 8, 12, 4), (1, 24, 10, 1)], patch=14, hidden=1280,
+                              head_dim=80, pixels="uniform")
+    wb = synth.small_workload(62, [(1, 10, 30, 1), (1, 32, 16, 1), (3, 6, 8, 6)], patch=14, hidden=1280,
+                              head_dim=80, pixels="uniform")
+    wb.W_bits, wb.b_bits = wa.W_bits, wa.b_bits          # one handle serves both
+    fe = _fe(wa)
+    ba, bb = fe.upload(wa.items), fe.upload(wb.items)
+    rows = max(ba.live_rows, bb.live_rows) + 200
+    hd, th = 80, wa.theta
+    ra = fe.embed_rope(ba, hd, th, rows=rows)
+    rb = fe.embed_rope(bb, hd, th, rows=rows)
+    torch.cuda.synchronize()
+    ref_a = [t.clone() for t in ra]
+    ref_b = [t.clone() for t in rb]
+    out = torch.full_like(ref_a[0], 7.0)
+    cos = torch.full_like(ref_a[1], 7.0)
+    sin = torch.full_like(ref_a[2], 7.0)
+    st = fe.status_tensor()
+    fe.embed_rope(ba, hd, th, rows=rows, out=out, cos=cos, sin=sin, status=st)
+    seen = out.clone()                                   # a torch kernel between two calls
+    for k in range(7):
+        fe.embed_rope(bb if k % 2 == 0 else ba, hd, th, rows=rows, out=out, cos=cos, sin=sin, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, -1]
+    assert np.array_equal(U.tensor_bits(seen), U.tensor_bits(ref_a[0]))
+    assert np.array_equal(U.tensor_bits(out), U.tensor_bits(ref_b[0]))
+    assert np.array_equal(cos.cpu().numpy(), ref_b[1].cpu().numpy())
+    assert np.array_equal(sin.cpu().numpy(), ref_b[2].cpu().numpy())
+    U.check_embed(_report(U.bits_to_f64(U.tensor_bits(out)), wb, U.item_starts(wb.items), bucket_rows=rows))
+    fe.close()
+
+
 def test_embed_rope_graph_replay_with_new_items():
     # one captured fused launch serves buckets whose items change between replays
     wl = synth.small_workload(31, [(1, 4, 6, 1), (2, 2, 4, 4), (1, 8, 8, 1)], patch=14, hidden=256, head_dim=80)

@@ -542,7 +542,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
-  write_status(args.status, &hs->tab);
+  // Every CTA is resident: the next call on the stream may start its prologue, A production
+  // and first passes now.  This kernel reads nothing another call writes (pixels, items,
+  // weights, bias, axis table); its global writes (embeddings, RoPE rows, status) wait for
+  // the previous kernel of the stream to finish (grid_dep_wait in the epilogue warps and
+  // before the timeout status below).
+  if (threadIdx.x == 0) grid_dep_trigger();
   const uint32_t tmem = hs->tmem_base;
   // barriers of the even CTA, through the cluster shared window
   const uint32_t a_full_L = mapa_shared(smem_u32(&hs->a_full[0]), 0);
@@ -907,6 +912,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const bool out32 = (reinterpret_cast<uintptr_t>(args.out) & 31u) == 0;
     uint32_t na = 0;
     bool ok = true;
+    // the first global write of this call: after the previous kernel of the stream
+    grid_dep_wait();
+    if (blockIdx.x == 0 && q == 0 && lane == 0 && args.status != nullptr) {
+      args.status[0] = hs->tab.code;
+      args.status[1] = hs->tab.bad_item;
+    }
     for (int u = cid; ok && u < args.num_units; u += ncl) {
       int tile, p_lo, p_hi;
       unit_range(args, u, tile, p_lo, p_hi);
@@ -997,6 +1008,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   if (warp == mma_warp<P>()) tmem_dealloc_pair(tmem, (uint32_t)args.tmem_cols);
   if (threadIdx.x == 0 && hs->abort_flag && args.status != nullptr) {
+    grid_dep_wait();
     args.status[0] = kTimeout;
     args.status[1] = -1;
   }
@@ -1107,11 +1119,20 @@ cudaError_t launch_embed(const Ctx& c, const uint8_t* pixels, int64_t pixel_byte
   int pairs = a.num_units < c.max_clusters ? a.num_units : c.max_clusters;
   if (pairs < 1) pairs = 1;
   const int grid = 2 * pairs;
-  if (c.P == 14)
-    embed_kernel<14><<<grid, kThreads, c.embed_smem, s>>>(c.tmap_w, c.tmap_wf, a);
-  else
-    embed_kernel<16><<<grid, kThreads, c.embed_smem, s>>>(c.tmap_w, c.tmap_wf, a);
-  return cudaGetLastError();
+  // programmatic stream serialization: the launch may begin while the previous kernel of the
+  // stream finishes (the kernel orders its own writes after it)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = c.embed_smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (c.P == 14) return cudaLaunchKernelEx(&cfg, embed_kernel<14>, c.tmap_w, c.tmap_wf, a);
+  return cudaLaunchKernelEx(&cfg, embed_kernel<16>, c.tmap_w, c.tmap_wf, a);
 }
 
 }  // namespace vitfe

@@ -217,6 +217,13 @@ __device__ __forceinline__ void decode_local(int local, int h, int w, int M, int
   ww = wb * M + mw;
 }
 
+// Programmatic dependent launch.  grid_dep_trigger: this CTA lets the next kernel of the
+// stream (launched with programmatic stream serialization) begin once every CTA of this grid
+// has triggered or exited.  grid_dep_wait: block until the previous kernel of the stream has
+// completed and its memory is visible (returns at once when there is none to wait for).
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Only CTA 0 writes the status pair; a timeout anywhere overrides it later.
 __device__ __forceinline__ void write_status(int32_t* status, const TabHdr* hdr) {
   if (status != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
