@@ -24,6 +24,14 @@
  *    its count) is read on the device at run time.
  *  - A handle serialises its own work: calls that share a handle must be
  *    ordered (one stream, or events between streams).
+ *  - The embedding calls (vitfe_embed, vitfe_embed_rope, vitfe_embed_folded)
+ *    launch with programmatic stream serialization: when the kernel before
+ *    one on its stream is another embedding launch, the call may start (read
+ *    its pixels, items and weights, produce and multiply) while that kernel
+ *    finishes, and every write it makes (outputs and status) waits for it.
+ *    So stream order holds for everything a call writes; inputs must not be
+ *    written by that previous embedding launch (none of them are), and a
+ *    kernel of the caller's before the call is waited for in full.
  *  - Host-side argument errors return a status and launch nothing.
  *    Device-side errors are written to the optional `status` word pair
  *    (int32[2] = {code, item index or -1}); every device call overwrites it
