@@ -294,7 +294,7 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
   // of the row in between
   VITFE_LOAD_ROW(R0);
   if (R0 + 1 <= RL && R0 + 1 < P) VITFE_LOAD_ROW(R0 + 1);
-  if (!mbar_wait_cl(a_empty0 + 8u * JB, empty_parity, abort_flag, limit_ns, 32)) return false;
+  if (!mbar_wait_cl(a_empty0 + 8u * JB, empty_parity, abort_flag, limit_ns)) return false;
   if (in_tmem<P>(JB)) tc_fence_after();
 
 #pragma unroll
@@ -358,7 +358,7 @@ __device__ __forceinline__ bool produce_blocks(const uint8_t* base, int64_t rs, 
           __syncwarp();
           if ((threadIdx.x & 31) == 0) mbar_arrive(a_local0 + 8u * (uint32_t)j);
           if (j + 1 < JE) {
-            if (!mbar_wait_cl(a_empty0 + 8u * (uint32_t)(j + 1), empty_parity, abort_flag, limit_ns, 32))
+            if (!mbar_wait_cl(a_empty0 + 8u * (uint32_t)(j + 1), empty_parity, abort_flag, limit_ns))
               return false;
             if (in_tmem<P>(j + 1)) tc_fence_after();
           }
@@ -621,8 +621,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int jj = 0; jj < NBLK; jj += 2) {
           const int j0 = blk_order<NBLK>(jj), j1 = blk_order<NBLK>(jj + 1);
-          if (!mbar_wait_warp<false>(a_local0 + 8u * (uint32_t)j0, np & 1u, abort_flag, args.limit_ns, 32) ||
-              !mbar_wait_warp<false>(a_local0 + 8u * (uint32_t)j1, np & 1u, abort_flag, args.limit_ns, 32)) {
+          if (!mbar_wait_warp<false>(a_local0 + 8u * (uint32_t)j0, np & 1u, abort_flag, args.limit_ns) ||
+              !mbar_wait_warp<false>(a_local0 + 8u * (uint32_t)j1, np & 1u, abort_flag, args.limit_ns)) {
             ok = false;
             break;
           }
