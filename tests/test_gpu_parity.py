@@ -501,6 +501,18 @@ def test_back_to_back_calls_into_one_buffer_keep_stream_order():
     assert np.array_equal(cos.cpu().numpy(), ref_b[1].cpu().numpy())
     assert np.array_equal(sin.cpu().numpy(), ref_b[2].cpu().numpy())
     U.check_embed(_report(U.bits_to_f64(U.tensor_bits(out)), wb, U.item_starts(wb.items), bucket_rows=rows))
+    # the RoPE expansion alone right after an embedding launch (which lets the next kernel
+    # start early) and in a chain of its own
+    c2 = torch.full_like(ref_a[1], 7.0)
+    s2 = torch.full_like(ref_a[2], 7.0)
+    fe.embed_rope(ba, hd, th, rows=rows, out=out, cos=cos, sin=sin, status=st)
+    for k in range(7):
+        fe.rope(bb if k % 2 == 0 else ba, hd, th, rows=rows, cos=c2, sin=s2, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, -1]
+    assert np.array_equal(c2.cpu().numpy(), ref_b[1].cpu().numpy())
+    assert np.array_equal(s2.cpu().numpy(), ref_b[2].cpu().numpy())
+    assert np.array_equal(U.tensor_bits(out), U.tensor_bits(ref_a[0]))
     fe.close()
 
 
