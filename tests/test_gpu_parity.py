@@ -181,6 +181,35 @@ def test_empty_and_all_pad_calls():
     fe.close()
 
 
+def test_max_items_in_one_call():
+    # VITFE_MAX_ITEMS small items (stills and a few videos): every pair tile holds rows of many
+    # items, and the kernels' item tables are full
+    from vit_vision_encoder_fusedinputnorm_gb300 import binding as B
+    grids = []
+    for i in range(B.VITFE_MAX_ITEMS):
+        if i % 16 == 5:
+            grids.append((2, 2, 4, 4))                        # a short video: t = 2 of 4 frames
+        else:
+            grids.append((1, 2 + 2 * (i % 3), 2 + 2 * (i % 4), 1))
+    wl = synth.small_workload(71, grids, patch=14, hidden=256, head_dim=80, pixels="uniform")
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    assert b.n_items.item() == B.VITFE_MAX_ITEMS
+    rows = b.live_rows + 100
+    st = fe.status_tensor()
+    out, cos, sin = fe.embed_rope(b, 80, wl.theta, rows=rows, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, -1]
+    rep = _report(U.bits_to_f64(U.tensor_bits(out)), wl, U.item_starts(wl.items), bucket_rows=rows)
+    U.log_report(f"{B.VITFE_MAX_ITEMS} items in one call: all {rep['rows']} rows", rep)
+    U.check_embed(rep)
+    assert np.all(U.tensor_bits(out)[b.live_rows:] == 0)
+    rc, rs = oracle.rope_workload(wl, bucket_rows=rows)
+    assert np.max(np.abs(cos.cpu().numpy() - rc)) <= U.ROPE_MAX_ABS
+    assert np.max(np.abs(sin.cpu().numpy() - rs)) <= U.ROPE_MAX_ABS
+    fe.close()
+
+
 def test_device_side_descriptor_errors_zero_the_item_rows():
     wl = synth.small_workload(13, [(1, 4, 4, 1), (1, 4, 6, 1), (1, 2, 2, 1)], patch=14, hidden=256)
     fe = _fe(wl)
