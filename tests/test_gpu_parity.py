@@ -210,6 +210,42 @@ def test_max_items_in_one_call():
     fe.close()
 
 
+def test_rope_side_limit():
+    # an item at the largest side the RoPE tables take (positions up to 4095), one just over
+    # it (rejected on the device by the fused call, its rows written as padding, but a valid
+    # item for the embeddings alone), and a small one after them
+    side = 4096
+    wl = synth.small_workload(73, [(1, 2, side, 1), (1, 2, side + 2, 1), (1, 4, 4, 1)], patch=14, hidden=256,
+                              head_dim=80, pixels="uniform")
+    fe = _fe(wl)
+    b = fe.upload(wl.items)
+    n0, n1 = 2 * side, 2 * (side + 2)
+    rows = b.live_rows + 20
+    st = fe.status_tensor()
+    out, cos, sin = fe.embed_rope(b, 80, wl.theta, rows=rows, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [4, 1]
+    o = U.bits_to_f64(U.tensor_bits(out))
+    c, sn = cos.cpu().numpy(), sin.cpu().numpy()
+    assert np.all(o[n0:n0 + n1] == 0) and np.all(c[n0:n0 + n1] == 1.0) and np.all(sn[n0:n0 + n1] == 0.0)
+    keep = np.r_[0:n0, n0 + n1:b.live_rows]
+    ok = [0, 2]
+    rep = U.embed_report(o[keep], oracle.embed_workload(wl, items=ok), oracle.embed_workload(wl, items=ok, bf16_input=True),
+                         U.item_starts([wl.items[i] for i in ok]))
+    U.log_report(f"item at the RoPE side limit ({side}): {rep['rows']} rows", rep)
+    U.check_embed(rep)
+    rc, rs = oracle.rope_workload(wl, items=ok)
+    assert np.max(np.abs(c[keep] - rc)) <= U.ROPE_MAX_ABS
+    assert np.max(np.abs(sn[keep] - rs)) <= U.ROPE_MAX_ABS
+    # the embeddings alone take the wider item
+    out2 = fe.embed(b, rows=rows, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, -1]
+    o2 = U.bits_to_f64(U.tensor_bits(out2))
+    U.check_embed(_report(o2, wl, U.item_starts(wl.items), bucket_rows=rows))
+    fe.close()
+
+
 def test_device_side_descriptor_errors_zero_the_item_rows():
     wl = synth.small_workload(13, [(1, 4, 4, 1), (1, 4, 6, 1), (1, 2, 2, 1)], patch=14, hidden=256)
     fe = _fe(wl)
