@@ -962,24 +962,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const int npw = min(args.bn, args.N - p * args.bn);
+        // fewer L1 wavefronts for the stores (the lanes swap halves, below) where the drain
+        // overlaps the next pass of a resident tile; where the drain is on the critical path
+        // (a unit's last pass, stream tiles' pass pairs) the shuffles would lengthen it
+        const bool swap = out32 && kind == kResident && p + 1 < p_hi;
         for (int c0 = 0; c0 < npw; c0 += 32) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + buf * (uint32_t)args.bn + (uint32_t)c0, v);
           tmem_wait_ld();
-          if (in_bucket) {
-            const int n0 = p * args.bn + c0;
-            uint32_t pk[16];
-            const float4* bias4 = reinterpret_cast<const float4*>(args.bias + n0);
+          const int n0 = p * args.bn + c0;
+          uint32_t pk[16];
+          const float4* bias4 = reinterpret_cast<const float4*>(args.bias + n0);
 #pragma unroll
-            for (int e4 = 0; e4 < 8; ++e4) {
-              const float4 bv = __ldg(bias4 + e4);
-              __nv_bfloat162 b0 = __floats2bfloat162_rn(__uint_as_float(v[4 * e4]) + bv.x,
-                                                        __uint_as_float(v[4 * e4 + 1]) + bv.y);
-              __nv_bfloat162 b1 = __floats2bfloat162_rn(__uint_as_float(v[4 * e4 + 2]) + bv.z,
-                                                        __uint_as_float(v[4 * e4 + 3]) + bv.w);
-              pk[2 * e4] = valid ? *reinterpret_cast<uint32_t*>(&b0) : 0u;
-              pk[2 * e4 + 1] = valid ? *reinterpret_cast<uint32_t*>(&b1) : 0u;
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 bv = __ldg(bias4 + e4);
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(__uint_as_float(v[4 * e4]) + bv.x,
+                                                      __uint_as_float(v[4 * e4 + 1]) + bv.y);
+            __nv_bfloat162 b1 = __floats2bfloat162_rn(__uint_as_float(v[4 * e4 + 2]) + bv.z,
+                                                      __uint_as_float(v[4 * e4 + 3]) + bv.w);
+            pk[2 * e4] = valid ? *reinterpret_cast<uint32_t*>(&b0) : 0u;
+            pk[2 * e4 + 1] = valid ? *reinterpret_cast<uint32_t*>(&b1) : 0u;
+          }
+          if (swap) {
+            // Lanes 2m and 2m+1 swap halves, so that each 256-bit store covers 64 contiguous
+            // bytes of a row (16 rows an instruction) rather than 32 bytes of 32 rows: the first
+            // store writes the even row of the pair, the second the odd one, the even lane the
+            // first 32 bytes of each and the odd lane the last 32.
+            const uint32_t odd = (uint32_t)lane & 1u;
+            uint32_t d1[8], d2[8];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+              const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? pk[w] : pk[8 + w], 1);
+              d1[w] = odd ? recv : pk[w];
+              d2[w] = odd ? pk[8 + w] : recv;
             }
+            const int re = r - (int)odd;                 // the pair's even row
+            __nv_bfloat16* dst = args.out + (size_t)re * (size_t)args.N + n0 + 16 * (int)odd;
+            if (re < args.rows) st_global_v8(dst, d1);
+            if (re + 1 < args.rows) st_global_v8(dst + args.N, d2);
+          } else if (in_bucket) {
             __nv_bfloat16* dst = orow + n0;
             if (out32) {
               st_global_v8(dst, pk);
