@@ -714,10 +714,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == mma_warp<P>()) {
     if (leader) {
       // The whole warp runs the issue loop, so its indices and descriptors stay warp-uniform
-      // (uniform registers); one elected lane issues each group of MMAs and its commit.
-      // Issue throughput of this one warp bounds the kernel, so the code between issues is
-      // minimal: descriptors at constant offsets, one poll and vote for barriers already
-      // complete.
+      // (uniform registers); one elected lane waits for each stage's weights and issues its
+      // MMAs and commit, and one vote per stage reconverges the warp.  The code between issues
+      // is kept minimal (descriptors at constant offsets, slow waits out of line): this one
+      // warp's issue time per stage has to stay under the stage's tensor time.
       uint32_t na = 0, np = 0, stage = 0, bphase = 0;
       bool ok = true;
       const uint64_t adesc0 = sw128_desc(a_smem);
